@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of physically sparse QSA decode on GB300.
+
+Workload: the long-context decode batch -- 8 independent queries, each with
+262,144 visible tokens (65,536 complete four-token groups), budget 512
+groups, indexer 8 heads x 64, GQA attention 16 query / 2 KV heads x 128, all
+values N(0,1), K/V in a wrapped ring buffer (slot = (t + 131,072) mod
+262,144).  One step = one pass of the whole hot path over the batch: group
+scoring, set choice + chronological emission, slot resolution + compact
+gather, online-softmax attention -- the four C-ABI stage calls that
+qsa_decode issues, with a CUDA event between stages.
+
+Timing: W untimed warm-up steps, then K timed steps.  Before each timed step
+L2 is flushed (a 256 MiB buffer written, then another 256 MiB read), outside
+the events; the step time is the device time between the events around its
+four launches.  Under torchrun every rank runs its own batch (weak scaling,
+no collective on the data path) and the slowest rank's time counts.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QSA decode queries/sec at 262,144 visible tokens; achieved HBM GB/s vs peak"
+UNIT = "queries/s"
+WORKLOAD = "long_262144"
+FLUSH_BYTES = 256 << 20
+PROFILE = os.path.join(ROOT, "profiles", "score_groups_long_262144.md")
+SCORE_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score.cu")
+
+
+def config_dict(w):
+    return {
+        "workload": WORKLOAD,
+        "batch_per_gpu": int(w.batch),
+        "visible_tokens": int(w.visible[0]),
+        "budget_groups": int(w.budget),
+        "indexer": f"{w.idx_heads} heads x {w.idx_dim}",
+        "attention": f"{w.q_heads} q / {w.kv_heads} kv heads x {w.head_dim}",
+        "slot_map": "ring buffer wrapped once: slot = (t + 131072) mod 262144",
+        "values": "N(0,1) float32, seeded",
+        "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
+    }
+
+
+def algorithmic_bytes(w):
+    """Bytes the method must move per query (raw index keys, selected K and
+    V rows, their slot-map entries, indexer and attention queries, output),
+    and the scorer's own per-launch bytes (raw keys + indexer query + scores)."""
+    per_q, scorer = [], 0
+    for b in range(w.batch):
+        T = int(w.visible[b])
+        G = T // 4
+        Wb = 4 * min(G, w.budget) + T % 4
+        per_q.append(T * w.idx_dim * 4 + Wb * w.kv_heads * w.head_dim * 4 * 2 + Wb * 4 +
+                     w.idx_heads * w.idx_dim * 4 + 2 * w.q_heads * w.head_dim * 4)
+        scorer += T * w.idx_dim * 4 + w.idx_heads * w.idx_dim * 4 + G * 4
+    return sum(per_q), scorer
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the scorer from the committed ncu summary, or
+    None if it is missing or was taken on a different scorer source."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = re.search(r"score_cu_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(SCORE_SRC, "rb").read()).hexdigest()
+    return int(m.group(1)) if cur == h.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from top_group_sparse_gb300 import workloads as wl
+    w = wl.long_262144()
+    t0 = time.perf_counter()
+    oracle.decode(w, queries=[0])
+    per_query = time.perf_counter() - t0
+    budget_s = 150.0
+    per_step = max(1, min(w.batch, int(budget_s / max(args.steps + args.warmup, 1) / per_query)))
+    queries = list(range(per_step))
+    for _ in range(args.warmup):
+        oracle.decode(w, queries=queries)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(w, queries=queries)
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} of the {w.batch} queries of the batch per step, "
+                                   f"single-threaded plain C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    if args.gpus != ws and ws > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {ws}")
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    from top_group_sparse_gb300 import build, qsa
+    from top_group_sparse_gb300 import workloads as wl
+    build.build()
+    qsa.load()
+
+    w = wl.long_262144(seed=4 + 1000 * rank)
+    db = qsa.DeviceBatch(w, device=f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+
+    # quick parity sample before timing: query 0's row against the oracle
+    db.decode()
+    st, flags = db.check_errors()
+    if st != 0:
+        raise SystemExit(f"device error word {flags:#x}")
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+        ref = oracle.decode(w, queries=[0])
+        n = int(ref["n_ids"][0])
+        ids_ok = int(db.n_ids[0]) == n and db.ids[0, :n].cpu().numpy().tobytes() == ref["ids"][0, :n].tobytes()
+        slots = w.slot_map[w.slot_offset[0] + ref["ids"][0, :n]]
+        err = float(np.abs(db.out[0].cpu().numpy() - ref["out"][0]).max() / np.abs(w.v_cache[slots]).max())
+        parity = {"query": 0, "ids_bit_exact": bool(ids_ok), "attn_err_rel_max_v": err}
+        if not ids_ok or err > 1e-5:
+            raise SystemExit(f"parity check failed: {parity}")
+
+    flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=db.out.device)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=db.out.device)
+    sink = torch.zeros(1, dtype=torch.float32, device=db.out.device)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=sink[0])
+
+    def step(ev=None):
+        if ev is None:
+            db.score(stream); db.select(stream); db.gather(stream); db.attend(stream)
+            return
+        ev[0].record(stream); db.score(stream)
+        ev[1].record(stream); db.select(stream)
+        ev[2].record(stream); db.gather(stream)
+        ev[3].record(stream); db.attend(stream)
+        ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        torch.cuda._sleep(20_000_000)  # let the launches queue ahead of the device
+        for k in range(K):
+            flush()
+            step(events[k])
+        torch.cuda.synchronize()
+        barrier()
+        loop_wall = time.perf_counter() - t0
+    st, flags = db.check_errors()
+    if st != 0:
+        raise SystemExit(f"device error word {flags:#x} after the timed loop")
+
+    step_ms = np.array([e[0].elapsed_time(e[4]) for e in events])
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in events])
+    total_ms = float(step_ms.sum())
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=db.out.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = ws * w.batch * K / (total_ms / 1e3)
+
+    # ---- end to end through qsa_decode with host buffers -----------------------
+    K2 = max(1, min(K, args.e2e_steps))
+    h_qidx = torch.from_numpy(w.q_idx).pin_memory()
+    h_q = torch.from_numpy(w.q).pin_memory()
+    h_vis = torch.from_numpy(w.visible).pin_memory()
+    h_koff = torch.from_numpy(w.key_offset).pin_memory()
+    h_soff = torch.from_numpy(w.slot_offset).pin_memory()
+    h_out = torch.empty(db.out.shape, dtype=torch.float32).pin_memory()
+    h_ids = torch.empty(db.ids.shape, dtype=torch.int32).pin_memory()
+    h_n = torch.empty(db.n_ids.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_qidx, h_q, h_vis, h_koff, h_soff))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_ids, h_n))
+
+    def e2e_step():
+        db.q_idx.copy_(h_qidx, non_blocking=True)
+        db.q.copy_(h_q, non_blocking=True)
+        db.visible.copy_(h_vis, non_blocking=True)
+        db.key_offset.copy_(h_koff, non_blocking=True)
+        db.slot_offset.copy_(h_soff, non_blocking=True)
+        db.decode(stream)
+        h_out.copy_(db.out, non_blocking=True)
+        h_ids.copy_(db.ids, non_blocking=True)
+        h_n.copy_(db.n_ids, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(K2):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=db.out.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = ws * w.batch * K2 / e2e_s
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- roofline of the dominant kernel (the scorer) --------------------------
+    path_bytes, scorer_bytes = algorithmic_bytes(w)
+    peak, peak_src = measured_peaks()
+    stage_mean = stage_ms.mean(axis=0)
+    score_gbs = scorer_bytes / (stage_mean[0] * 1e-3) / 1e9
+    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        sample = list(range(w.batch))
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.decode(w, queries=sample)
+            reps += 1
+            if time.perf_counter() - t0 > 8.0 or reps >= 4:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * len(sample) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps} pass(es) over all {len(sample)} queries of the batch, "
+                         f"single-threaded plain C oracle, {dt:.1f} s"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_dict(w),
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                   "reasons": clocks["reasons"], "samples": clocks["samples"]},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "note": "qsa_decode per step; queries copied in from pinned host memory, ID rows "
+                        "and outputs copied back, stream synchronised; K/V cache and index-key "
+                        "history resident in HBM"},
+        "gpu_launches": 4 * K,
+        "roofline": {"kernel": "score_groups", "bound": "hbm", "achieved": score_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": score_gbs / peak,
+                     "traffic": profile_traffic(),
+                     "note": f"algorithmic bytes {scorer_bytes} per launch (raw index keys + "
+                             f"indexer queries + scores), peak = {peak_src} HBM copy bandwidth"},
+        "path_hbm": {"achieved_gbs": path_gbs, "frac_of_measured": path_gbs / peak,
+                     "frac_of_8tbs": path_gbs / 8000.0, "algorithmic_bytes_per_step": path_bytes},
+        "stages_us": {n: float(v * 1e3) for n, v in
+                      zip(("score", "select", "gather", "attend"), stage_mean)},
+        "loop_wall_s": loop_wall,
+        "parity_sample": parity,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

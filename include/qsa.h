@@ -1,0 +1,214 @@
+/*
+ * qsa.h -- C ABI of libqsa, physically sparse QSA decode on GB300 (sm_103a).
+ *
+ * The method is the one defined by two notes of the Hebrus project:
+ *   [AFN-017] "Top-k chooses the set; time chooses the order"
+ *   [AFN-016] "A sparse mask is not sparse attention"
+ * Per decode query with T visible tokens, the path
+ *   scores every complete four-token group g (tokens 4g..4g+3) as
+ *     sum over indexer heads h of ReLU(q_h . mean(k_4g..k_4g+3)),
+ *   chooses the top min(G, budget) groups by (score desc, position asc),
+ *   emits them in ascending position, each expanded to 4 token IDs, and
+ *     appends the raw tail of T mod 4 tokens (at most 2,051 IDs),
+ *   resolves the IDs through a slot map, gathers only those K/V rows into
+ *     bounded scratch, and
+ *   runs an online softmax over that compact row in emitted order.
+ * No query-by-key mask is ever built ([AFN-016] What the checkpoint measures).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All pointers except `dims`, `stats` and host-side arguments named
+ *   `*_host` are DEVICE pointers of the current CUDA device.  The library
+ *   never allocates or frees memory: the caller owns every buffer,
+ *   including the workspace ([AFN-016] What the checkpoint measures: byte
+ *   ownership is visible).
+ * - Float arrays are IEEE binary32, row-major, and must start on a 16-byte
+ *   boundary; the workspace on a 256-byte boundary.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *   compute call is asynchronous on `stream` and returns after enqueueing.
+ * - Host-detectable errors (NULL or misaligned pointers, bad dimensions,
+ *   unsupported shapes, a workspace that is too small) return a status
+ *   before anything is enqueued.  A failed launch returns QSA_ERR_CUDA.
+ * - Errors that only the device can see (a T_b outside [0, max_visible],
+ *   a slot outside [0, num_slots), an ID row longer than its capacity, a
+ *   bounded wait that ran out) never trap: the kernel skips the bad access,
+ *   writes zeros / an empty row for that query, and sets a bit in a sticky
+ *   error word in the workspace, which qsa_check_errors() reads and clears.
+ * - Results are deterministic: the same inputs give bit-identical outputs,
+ *   whatever the batch composition or the number of SMs.
+ * - Calls that share one workspace must not overlap on the GPU.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1,          /* NULL/misaligned pointer, bad value     */
+    QSA_ERR_UNSUPPORTED_SHAPE = 2,    /* no kernel built for these dimensions  */
+    QSA_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < qsa_workspace_size(dims)   */
+    QSA_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed  */
+    QSA_ERR_DEVICE_FAULT = 5          /* the device error word was non-zero    */
+} qsa_status;
+
+/* Bits of the device error word (see qsa_check_errors). */
+#define QSA_DEVERR_VISIBLE_RANGE 0x1u  /* some T_b < 0 or T_b > max_visible   */
+#define QSA_DEVERR_SLOT_RANGE    0x2u  /* a slot-map entry outside the cache  */
+#define QSA_DEVERR_ROW_RANGE     0x4u  /* n_ids[b] or an ID outside its row   */
+#define QSA_DEVERR_WAIT_TIMEOUT  0x8u  /* a bounded copy wait ran out         */
+
+/* Problem dimensions.  Supported builds: (idx_heads, idx_dim) in
+ * {(4,32), (8,32), (4,64), (8,64)}; head_dim in {64, 128};
+ * q_heads = kv_heads * r with r in 1..16; group == 4; 1 <= budget_groups
+ * <= 512; 0 <= max_visible <= QSA_MAX_VISIBLE. */
+typedef struct {
+    int32_t batch;          /* B: decode queries in this call (>= 0)              */
+    int32_t idx_heads;      /* H_I: indexer query heads                          */
+    int32_t idx_dim;        /* d_I: width of one raw index key                   */
+    int32_t q_heads;        /* n_q: attention query heads                        */
+    int32_t kv_heads;       /* n_kv: K/V heads; q head h reads KV head h/(n_q/n_kv) */
+    int32_t head_dim;       /* d: attention head width                           */
+    int32_t group;          /* tokens per scored group; must be 4 ([AFN-017] Decision) */
+    int32_t budget_groups;  /* groups kept per query; 512 in the notes           */
+    int32_t max_visible;    /* upper bound on every T_b; sizes scores and grids  */
+    float scale;            /* softmax scale, usually 1/sqrt(head_dim)           */
+} qsa_dims;
+
+#define QSA_MAX_VISIBLE (1 << 26)
+#define QSA_MAX_BUDGET 512
+
+/* Inputs of one decode batch (device pointers). */
+typedef struct {
+    const float *q_idx;          /* [B, H_I, d_I] indexer queries                        */
+    const float *idx_keys;       /* [total_tokens, d_I] raw index keys, LOGICAL order:   */
+                                 /*   query b's token t is row key_offset[b] + t         */
+    const int64_t *key_offset;   /* [B] first row of query b's history in idx_keys       */
+    const int32_t *visible;      /* [B] T_b, visible tokens of query b                   */
+    const float *q;              /* [B, n_q, d] attention queries                        */
+    const float *k_cache;        /* [num_slots, n_kv, d] K rows by PHYSICAL slot         */
+    const float *v_cache;        /* [num_slots, n_kv, d] V rows by PHYSICAL slot         */
+    int64_t num_slots;           /* physical slots in k_cache / v_cache                  */
+    const int32_t *slot_map;     /* logical -> physical: query b's token t lives in slot */
+                                 /*   slot_map[slot_offset[b] + t]                        */
+    const int64_t *slot_offset;  /* [B] first slot-map entry of query b's history        */
+} qsa_inputs;
+
+/* Work and byte ownership of one batch ([AFN-016] What the checkpoint
+ * measures: candidate groups scored, selected groups and expanded width,
+ * raw-key / K/V / pooled-key / workspace / total bytes, zero dense mask). */
+typedef struct {
+    int64_t candidate_groups;   /* sum_b floor(T_b/4)                            */
+    int64_t selected_groups;    /* sum_b min(floor(T_b/4), budget)               */
+    int64_t selected_tokens;    /* sum_b (4*selected groups + T_b mod 4)         */
+    int64_t raw_key_bytes;      /* index-key bytes the scorer reads              */
+    int64_t kv_bytes;           /* K and V bytes the gather reads                */
+    int64_t pooled_key_bytes;   /* pooled keys kept in device memory: 0 (they    */
+                                /*   live in shared memory only)                 */
+    int64_t workspace_bytes;    /* qsa_workspace_size(dims)                      */
+    int64_t total_bytes;        /* raw_key + kv + pooled_key + workspace         */
+    int64_t dense_mask_bytes;   /* bytes of any query-by-key mask: always 0      */
+} qsa_stats;
+
+/* ---- sizes (host only, no CUDA call) ---------------------------------- */
+
+/* Bytes of workspace every call below needs for these dims (0 if the dims
+ * are invalid).  Sized as groups + budget + selected width per query,
+ * never queries x keys ([AFN-016] What the checkpoint measures):
+ *   header + B*score_stride*4 (scores) + 2*B*row_capacity*n_kv*d*4 (K/V
+ *   scratch) + B*n_q*ceil(row_capacity/64)*(d+2)*4 (attention partials). */
+size_t qsa_workspace_size(const qsa_dims *dims);
+
+/* Row stride, in floats, of a scores buffer: max_visible/4 rounded up to 32. */
+int64_t qsa_score_stride(const qsa_dims *dims);
+
+/* Capacity of one emitted ID row: 4*budget_groups + 3 (2,051 at budget 512,
+ * [AFN-016] Decision). */
+int32_t qsa_row_capacity(const qsa_dims *dims);
+
+/* Fills *out from the dims and the host copy of visible ([B] T_b). */
+qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_stats *out);
+
+const char *qsa_status_string(qsa_status status);
+
+/* ---- workspace ---------------------------------------------------------- */
+
+/* Zeroes the workspace header (error word and attention tickets).  Call once
+ * after allocating a workspace, before its first use; a zero-filled
+ * allocation needs no call.  Afterwards every call leaves the header clean. */
+qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the sticky device error word
+ * of `ws`.  *flags_out (may be NULL) receives the QSA_DEVERR_* bits.
+ * Returns QSA_ERR_DEVICE_FAULT if any bit was set, else QSA_OK. */
+qsa_status qsa_check_errors(void *ws, size_t ws_bytes, void *stream, uint32_t *flags_out);
+
+/* ---- the hot path, one stage per call ----------------------------------- */
+
+/* Stage 1 -- group scoring ([AFN-016] Decision: score complete groups in
+ * bounded tiles; Why a sparse mask can still be dense: pooled groups and
+ * sum(ReLU(dot_h))).  For each query b and each complete group
+ * g < floor(T_b/4):
+ *   p[j] = (((k[4g][j] + k[4g+1][j]) + k[4g+2][j]) + k[4g+3][j]) * 0.25
+ *   scores[b*score_stride + g] = sum_{h=0..H_I-1, in order} ReLU(dot_h),
+ *   dot_h = fma chain over j = 0..d_I-1 starting from +0, ReLU(x) = x>0 ? x : +0,
+ * every step binary32 round-to-nearest in exactly that order, so scores are
+ * bit-identical to any implementation of that order.
+ * scores: [B, qsa_score_stride(dims)]; entries g >= floor(T_b/4) untouched. */
+qsa_status qsa_score_groups(const qsa_dims *dims, const qsa_inputs *in, float *scores,
+                            void *ws, size_t ws_bytes, void *stream);
+
+/* Stage 2 -- set choice and chronological emission ([AFN-017] Decision;
+ * Tie handling belongs to membership).  Chooses the top
+ * k = min(floor(T_b/4), budget) groups of scores[b] by (score descending,
+ * group position ascending) -- ties resolved while choosing membership --
+ * then writes their IDs in ascending logical position, each group expanded
+ * to 4 consecutive token IDs, followed by the raw tail 4*floor(T_b/4)..T_b-1:
+ *   ids:   [B, qsa_row_capacity(dims)] int32, entries >= n_ids[b] untouched
+ *   n_ids: [B] int32, = 4k + T_b mod 4
+ * Scores must not be NaN (-0 counts as +0).  Below budget the row is exactly
+ * 0..T_b-1, the dense causal row ([AFN-017] The dense-parity property). */
+qsa_status qsa_select(const qsa_dims *dims, const int32_t *visible, const float *scores,
+                      int32_t *ids, int32_t *n_ids, void *ws, size_t ws_bytes, void *stream);
+
+/* Stage 3 -- slot resolution and compact gather ([AFN-016] Decision: only
+ * the gather crosses from logical identity into the physical layout; Why
+ * compact gather comes before fusion).  For i < n_ids[b]:
+ *   s = slot_map[slot_offset[b] + ids[b][i]]
+ *   k_scr[b][i][:][:] = k_cache[s][:][:],  v_scr[b][i][:][:] = v_cache[s][:][:]
+ * k_scr, v_scr: [B, qsa_row_capacity(dims), n_kv, d]; rows >= n_ids[b]
+ * untouched.  A slot outside [0, num_slots) zero-fills that row and sets
+ * QSA_DEVERR_SLOT_RANGE. */
+qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids,
+                      const int32_t *n_ids, float *k_scr, float *v_scr,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/* Stage 4 -- online softmax over the compact row ([AFN-017] Floating point
+ * makes order observable; [AFN-016] Decision).  For each query b and head h
+ * (KV head h / (n_q/n_kv)):
+ *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
+ * rows i < n_ids[b] visited in emitted order: the row is cut into fixed
+ * 64-row chunks, each reduced with a running max / rescale / denominator /
+ * accumulator, and the chunk partials merged in ascending chunk order.  The
+ * split depends only on n_ids[b], so results do not depend on the batch.
+ * n_ids[b] = 0 gives a zero output.  out: [B, n_q, d]. */
+qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr,
+                      const float *v_scr, const int32_t *n_ids, float *out,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/* The whole path -- stages 1-4 back to back on `stream`, with scores and K/V
+ * scratch kept in the workspace.  Outputs: ids, n_ids (as qsa_select) and
+ * out (as qsa_attend). */
+qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
+                      int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,134 @@
+"""The C-ABI library builds, loads and exports every symbol include/qsa.h
+declares; its host-only logic (sizes, stats, validation) runs without a GPU.
+No call here reaches a CUDA kernel: every compute call below is rejected by
+host-side validation before anything is enqueued."""
+import ctypes
+
+import pytest
+
+from top_group_sparse_gb300 import build as qbuild
+from top_group_sparse_gb300 import qsa
+
+QSA_OK, INVALID, UNSUPPORTED, WS_SMALL = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qsa.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = qsa.exported_symbols()
+    assert len(names) == 12
+    for n in names:
+        assert hasattr(lib, n), n
+    for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode"):
+        assert n in names
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert len(qsa.qsa_status_string(s)) >= 2
+    assert qsa.qsa_status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(batch=8, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2, head_dim=128,
+                budget_groups=512, max_visible=262144)
+    base.update(kw)
+    return qsa.make_dims(**base)
+
+
+def test_row_capacity_and_score_stride(lib):
+    assert qsa.qsa_row_capacity(_dims()) == 2051
+    assert qsa.qsa_row_capacity(_dims(budget_groups=1)) == 7
+    assert qsa.qsa_score_stride(_dims()) == 65536
+    assert qsa.qsa_score_stride(_dims(max_visible=65537)) == 16384
+    assert qsa.qsa_score_stride(_dims(max_visible=37)) == 32
+    assert qsa.qsa_score_stride(_dims(max_visible=0)) == 32
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def test_workspace_formula(lib):
+    """Scratch is groups + budget + selected width per query, never queries x
+    keys ("A sparse mask is not sparse attention", What the checkpoint measures)."""
+    d = _dims()
+    B, nq, nkv, hd, cap = 8, 16, 2, 128, 2051
+    nch = -(-cap // 64)
+    want = 256 + _align(B * nkv * 4) + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
+        + _align(B * 65536 * 4) + 2 * _align(B * cap * nkv * hd * 4)
+    assert qsa.qsa_workspace_size(d) == want
+    # doubling the history adds exactly the scores of the new groups
+    a = qsa.qsa_workspace_size(_dims(max_visible=1 << 20))
+    b = qsa.qsa_workspace_size(_dims(max_visible=1 << 21))
+    assert b - a == B * ((1 << 19) - (1 << 18)) * 4
+    # and is linear in the batch
+    assert qsa.qsa_workspace_size(_dims(batch=16)) < 2 * qsa.qsa_workspace_size(d) + 4096
+
+
+def test_invalid_dims_give_zero_workspace(lib):
+    assert qsa.qsa_workspace_size(_dims(group=3)) == 0
+    assert qsa.qsa_workspace_size(_dims(budget_groups=0)) == 0
+    assert qsa.qsa_workspace_size(_dims(budget_groups=513)) == 0
+    assert qsa.qsa_workspace_size(_dims(q_heads=15)) == 0
+    assert qsa.qsa_workspace_size(_dims(batch=-1)) == 0
+    assert qsa.qsa_workspace_size(_dims(max_visible=(1 << 26) + 1)) == 0
+
+
+def test_stats_closed_forms(lib):
+    d = _dims(batch=4, max_visible=300000)
+    vis = [0, 37, 2052, 262144]
+    st = qsa.qsa_get_stats(d, vis)
+    G = [0, 9, 513, 65536]
+    k = [0, 9, 512, 512]
+    W = [0, 37, 2048, 2048]
+    assert st["candidate_groups"] == sum(G)
+    assert st["selected_groups"] == sum(k)
+    assert st["selected_tokens"] == sum(W)
+    assert st["raw_key_bytes"] == sum(vis) * 64 * 4
+    assert st["kv_bytes"] == sum(W) * 2 * 128 * 4 * 2
+    assert st["pooled_key_bytes"] == 0
+    assert st["workspace_bytes"] == qsa.qsa_workspace_size(d)
+    assert st["total_bytes"] == st["raw_key_bytes"] + st["kv_bytes"] + st["workspace_bytes"]
+    assert st["dense_mask_bytes"] == 0
+    with pytest.raises(qsa.QsaError):
+        qsa.qsa_get_stats(d, [0, 1, 2, 300001])
+
+
+def _raw(fn, *args):
+    return getattr(qsa.load(), fn)(*args)
+
+
+def test_validation_rejects_before_launch(lib):
+    """Every one of these returns a status without touching the GPU."""
+    d = _dims(batch=2, max_visible=4096)
+    bad = _dims(group=5)
+    fake = 1 << 20  # 256-aligned non-null address that is never dereferenced
+    inp = qsa.QsaInputs(fake, fake, fake, fake, fake, fake, fake, 100, fake, fake)
+    null_inp = qsa.QsaInputs(None, fake, fake, fake, fake, fake, fake, 100, fake, fake)
+    mis_inp = qsa.QsaInputs(fake + 4, fake, fake, fake, fake, fake, fake, 100, fake, fake)
+    ws_need = qsa.qsa_workspace_size(d)
+    D, I = ctypes.byref, ctypes.byref
+    assert _raw("qsa_decode", D(bad), I(inp), fake, fake, fake, fake, ws_need, None) == INVALID
+    assert _raw("qsa_decode", D(d), I(null_inp), fake, fake, fake, fake, ws_need, None) == INVALID
+    assert _raw("qsa_decode", D(d), I(mis_inp), fake, fake, fake, fake, ws_need, None) == INVALID
+    assert _raw("qsa_decode", D(d), I(inp), fake, fake, fake, fake, ws_need - 1, None) == WS_SMALL
+    assert _raw("qsa_decode", D(d), I(inp), fake, fake, fake, fake + 8, ws_need, None) == INVALID
+    assert _raw("qsa_decode", D(d), I(inp), None, fake, fake, fake, ws_need, None) == INVALID
+    uns = _dims(batch=2, max_visible=4096, idx_dim=48)
+    assert _raw("qsa_decode", D(uns), I(inp), fake, fake, fake, fake, 1 << 30, None) == UNSUPPORTED
+    uns = _dims(batch=2, max_visible=4096, head_dim=96)
+    assert _raw("qsa_attend", D(uns), fake, fake, fake, fake, fake, fake, 1 << 30, None) == UNSUPPORTED
+    uns = _dims(batch=2, max_visible=4096, q_heads=64, kv_heads=2)
+    assert _raw("qsa_attend", D(uns), fake, fake, fake, fake, fake, fake, 1 << 30, None) == UNSUPPORTED
+    assert _raw("qsa_score_groups", D(d), I(inp), None, fake, ws_need, None) == INVALID
+    assert _raw("qsa_select", D(d), fake, fake, None, fake, fake, ws_need, None) == INVALID
+    assert _raw("qsa_select", D(d), fake, fake + 4, fake, fake, fake, ws_need, None) == INVALID
+    assert _raw("qsa_gather", D(d), I(inp), fake, fake, fake, fake + 4, fake, ws_need, None) == INVALID
+    assert _raw("qsa_attend", D(d), fake, fake, fake, fake, fake, fake, 100, None) == WS_SMALL
+    assert _raw("qsa_workspace_init", None, 10, None) == INVALID
+    assert _raw("qsa_check_errors", fake, 8, None, None) == INVALID

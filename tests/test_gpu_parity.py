@@ -1,0 +1,182 @@
+"""GPU parity of every stage against the CPU oracle, through the C ABI.
+
+Sizes here finish in the oracle within seconds yet span many scorer tiles,
+several select-cluster slices, several attention chunks and ragged tails."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from gpu_helpers import (full_parity, need_gpu, oracle_run, run_decode, run_stages,
+                         assert_ids_equal, assert_attention_close)
+from top_group_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_t37_dense_row():
+    """37 visible tokens: 9 groups + 1 tail, below budget, row = 0..36."""
+    w = wl.single_t37()
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+    assert gpu["ids"][0, :37].tolist() == list(range(37))
+
+
+def test_dense_parity_sweep_with_ties():
+    """T in {0..5, 2047..2052} on the exact k/8 grid: byte-identical dense rows
+    below the cut; at 2052 the tie rule picks the dropped group."""
+    w = wl.dense_parity_sweep()
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+    for b, T in enumerate(w.visible.tolist()):
+        if T <= 2051:
+            assert gpu["ids"][b, :T].tobytes() == np.arange(T, dtype=np.int32).tobytes()
+    dec = run_decode(w)
+    assert dec["ids"].tobytes() == gpu["ids"].tobytes()
+    assert dec["out"].tobytes() == gpu["out"].tobytes()
+
+
+@pytest.mark.parametrize("T", [2052, 2053, 2055, 4 * 513 + 3, 9001, 20003])
+def test_paged_gqa_multi_tile(T):
+    """GQA 16/2 x 128 with 16-token pages, several T around and above the cut."""
+    w = wl.make_workload("paged", [T, T - 1, max(T - 5, 0)], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=T, slots="paged16")
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+
+
+def test_ragged_batch_all_edges():
+    """One batch mixing empty, tail-only, exactly-budget, budget+1 and long rows."""
+    vis = [0, 1, 2, 3, 4, 7, 2047, 2048, 2051, 2052, 2053, 4 * 600 + 1, 33333, 65537]
+    w = wl.make_workload("ragged", vis, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2,
+                         head_dim=128, seed=77, slots="permutation")
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+    assert np.all(gpu["out"][0] == 0)
+
+
+@pytest.mark.parametrize("shape", [(4, 32, 2, 2, 64), (8, 32, 4, 1, 64), (4, 64, 8, 8, 128),
+                                   (8, 64, 16, 1, 128)])
+def test_every_built_shape(shape):
+    """Each compiled (H_I, d_I) scorer and head_dim / GQA attention variant."""
+    H, dI, nq, nkv, hd = shape
+    w = wl.make_workload("shape", [5003, 12000, 2052], idx_heads=H, idx_dim=dI, q_heads=nq,
+                         kv_heads=nkv, head_dim=hd, seed=H * dI + nq, slots="permutation")
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+
+
+@pytest.mark.parametrize("budget", [1, 2, 7, 100, 511, 512])
+def test_budgets(budget):
+    w = wl.make_workload("budget", [4 * 700 + 2, 3001, 4 * budget, 4 * budget + 4], idx_heads=4,
+                         idx_dim=32, q_heads=2, kv_heads=2, head_dim=64, seed=budget,
+                         slots="identity", budget=budget)
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    assert gpu["status"] == 0
+    full_parity(w, gpu, ref)
+
+
+def test_all_scores_tie():
+    """Identical index keys: every group scores the same, membership is the
+    first `budget` groups (smaller positions win)."""
+    w = wl.make_workload("ties", [9000, 4 * 513, 20001], idx_heads=4, idx_dim=32, q_heads=2,
+                         kv_heads=2, head_dim=64, seed=3)
+    w = dataclasses.replace(w, idx_keys=np.repeat(w.idx_keys[:1], w.total_tokens, axis=0))
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    full_parity(w, gpu, ref)
+    for b, T in enumerate(w.visible.tolist()):
+        assert gpu["ids"][b, :2048].tolist() == list(range(2048))
+
+
+def test_zero_scores_everywhere():
+    """An all-zero indexer query: every dot is 0, every ReLU +0, all tie."""
+    w = wl.make_workload("zeros", [6000, 2053], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=4)
+    w = dataclasses.replace(w, q_idx=np.zeros_like(w.q_idx))
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    full_parity(w, gpu, ref)
+    assert np.all(gpu["scores"][0, :1500] == 0)
+
+
+def test_heavy_ties_on_integer_grid_long():
+    """k/8 grid values over a long history: many exact ties at the threshold."""
+    w = wl.make_workload("grid", [40000, 40001, 40003], idx_heads=4, idx_dim=32, q_heads=2,
+                         kv_heads=2, head_dim=64, seed=12, index_values="grid8",
+                         history="shared", slots="permutation")
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    full_parity(w, gpu, ref)
+    s = ref["scores"][0, :10000]
+    assert len(np.unique(s)) < 2000  # the ties are really there
+
+
+def test_select_uncached_long_history():
+    """A history long enough that a cluster slice of scores no longer fits in
+    shared memory (G > 8 * 49152), so select streams scores from global."""
+    T = 8 * 49152 * 4 + 4 * 1000 + 2
+    w = wl.make_workload("long", [T], idx_heads=4, idx_dim=32, q_heads=2, kv_heads=2,
+                         head_dim=64, seed=13, slots="ring", ring_size=T, ring_shift=777)
+    gpu = run_stages(w)
+    ref = oracle_run(w)
+    full_parity(w, gpu, ref)
+
+
+def test_decode_matches_stages_and_is_repeatable():
+    w = wl.make_workload("rep", [30001, 4 * 512 + 1, 17], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=31, slots="paged16")
+    st = run_stages(w)
+    d1 = run_decode(w)
+    d2 = run_decode(w, db=d1["batch"])
+    for k in ("ids", "n_ids", "out"):
+        assert d1[k].tobytes() == st[k].tobytes(), k
+        assert d2[k].tobytes() == d1[k].tobytes(), k
+
+
+def test_chunk_equals_decode_small():
+    """Consecutive queries over one history equal single-query decodes, bit
+    for bit (the attention split depends on the row length only)."""
+    w = wl.chunked_prefill_100000(n=24, first=9000)
+    chunk = run_decode(w)
+    ref = oracle_run(w)
+    assert_ids_equal(w, chunk, ref)
+    assert_attention_close(w, chunk, ref)
+    for b in range(w.batch):
+        one = run_decode(w.subset([b]))
+        n = int(one["n_ids"][0])
+        assert n == int(chunk["n_ids"][b])
+        assert one["ids"][0, :n].tobytes() == chunk["ids"][b, :n].tobytes()
+        assert one["out"][0].tobytes() == chunk["out"][b].tobytes()
+
+
+def test_non_default_stream():
+    torch = need_gpu()
+    w = wl.make_workload("stream", [9000, 2051], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=41)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gpu = run_stages(w, stream=s)
+    ref = oracle_run(w)
+    full_parity(w, gpu, ref)
+
+
+def test_stats_report_zero_dense_mask():
+    need_gpu()
+    from top_group_sparse_gb300 import qsa
+    w = wl.single_t37()
+    db = qsa.DeviceBatch(w)
+    st = qsa.qsa_get_stats(db.dims, w.visible)
+    assert st["dense_mask_bytes"] == 0
+    assert st["selected_tokens"] == 37 and st["candidate_groups"] == 9

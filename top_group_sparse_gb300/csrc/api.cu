@@ -1,0 +1,331 @@
+// api.cu -- the extern "C" boundary of libqsa (declared in include/qsa.h).
+//
+// Host side only: argument validation (every host-detectable error returns a
+// status before anything is enqueued), the workspace layout, and the launch
+// of each stage's kernel on the caller's stream.  The library allocates
+// nothing; all buffers, the workspace included, belong to the caller.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+bool dims_valid(const qsa_dims *d)
+{
+    if (!d) return false;
+    if (d->batch < 0 || d->batch > 65535) return false;
+    if (d->group != kGroup) return false;
+    if (d->budget_groups < 1 || d->budget_groups > QSA_MAX_BUDGET) return false;
+    if (d->max_visible < 0 || d->max_visible > QSA_MAX_VISIBLE) return false;
+    if (d->idx_heads <= 0 || d->idx_dim <= 0 || d->q_heads <= 0 || d->kv_heads <= 0 || d->head_dim <= 0)
+        return false;
+    if (d->q_heads % d->kv_heads != 0) return false;
+    if (!(d->scale == d->scale)) return false;  // NaN scale
+    return true;
+}
+
+Layout make_layout(const qsa_dims *d)
+{
+    Layout L{};
+    const int64_t gmax = d->max_visible / kGroup;
+    L.score_stride = ((gmax + 31) / 32) * 32;
+    if (L.score_stride == 0) L.score_stride = 32;
+    L.row_cap = kGroup * d->budget_groups + (kGroup - 1);
+    L.nchunk_max = (L.row_cap + kAttendChunk - 1) / kAttendChunk;
+    const size_t B = size_t(d->batch);
+    size_t off = 0;
+    L.off_err = off;
+    off += kWsAlign;
+    L.off_tickets = off;
+    off = align_up(off + B * size_t(d->kv_heads) * 4, kWsAlign);
+    const size_t nparts = B * size_t(d->q_heads) * size_t(L.nchunk_max);
+    L.off_part_m = off;
+    off = align_up(off + nparts * 4, kWsAlign);
+    L.off_part_l = off;
+    off = align_up(off + nparts * 4, kWsAlign);
+    L.off_part_acc = off;
+    off = align_up(off + nparts * size_t(d->head_dim) * 4, kWsAlign);
+    L.off_scores = off;
+    off = align_up(off + B * size_t(L.score_stride) * 4, kWsAlign);
+    const size_t scr = B * size_t(L.row_cap) * size_t(d->kv_heads) * size_t(d->head_dim) * 4;
+    L.off_kscr = off;
+    off = align_up(off + scr, kWsAlign);
+    L.off_vscr = off;
+    off = align_up(off + scr, kWsAlign);
+    L.total = off;
+    return L;
+}
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int num_sms_of_current_device()
+{
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+qsa_status check_ws(const qsa_dims *d, void *ws, size_t ws_bytes)
+{
+    if (!ws || !aligned(ws, kWsAlign)) return QSA_ERR_INVALID_ARG;
+    if (ws_bytes < make_layout(d).total) return QSA_ERR_WORKSPACE_TOO_SMALL;
+    return QSA_OK;
+}
+
+qsa_status check_inputs_score(const qsa_inputs *in)
+{
+    if (!in || !in->q_idx || !in->idx_keys || !in->key_offset || !in->visible) return QSA_ERR_INVALID_ARG;
+    if (!aligned(in->q_idx, 16) || !aligned(in->idx_keys, 16) || !aligned(in->key_offset, 8) ||
+        !aligned(in->visible, 4))
+        return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
+qsa_status check_inputs_gather(const qsa_inputs *in)
+{
+    if (!in || !in->visible || !in->k_cache || !in->v_cache || !in->slot_map || !in->slot_offset)
+        return QSA_ERR_INVALID_ARG;
+    if (in->num_slots < 0) return QSA_ERR_INVALID_ARG;
+    if (!aligned(in->k_cache, 16) || !aligned(in->v_cache, 16) || !aligned(in->slot_map, 4) ||
+        !aligned(in->slot_offset, 8) || !aligned(in->visible, 4))
+        return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
+qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
+
+uint32_t *err_word(void *ws, const Layout &L)
+{
+    return reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(ws) + L.off_err);
+}
+
+template <typename T>
+T *ws_at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<unsigned char *>(ws) + off);
+}
+
+qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int64_t stride, void *ws,
+                    const Layout &L, cudaStream_t s)
+{
+    if (d->batch == 0) return QSA_OK;
+    const int sms = num_sms_of_current_device();
+    if (sms <= 0) return QSA_ERR_CUDA;
+    ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, stride,
+                d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L)};
+    return from_cuda(launch_score(a, sms, s));
+}
+
+qsa_status do_select(const qsa_dims *d, const int32_t *visible, const float *scores, int64_t stride,
+                     int32_t *ids, int32_t *n_ids, void *ws, const Layout &L, cudaStream_t s)
+{
+    if (d->batch == 0) return QSA_OK;
+    SelectArgs a{visible, scores, stride, ids, n_ids, L.row_cap, d->budget_groups, d->max_visible,
+                 d->batch, err_word(ws, L)};
+    return from_cuda(launch_select(a, s));
+}
+
+qsa_status do_gather(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
+                     float *k_scr, float *v_scr, void *ws, const Layout &L, cudaStream_t s)
+{
+    if (d->batch == 0) return QSA_OK;
+    GatherArgs a{in->visible, ids, n_ids, in->slot_map, in->slot_offset, in->k_cache, in->v_cache,
+                 in->num_slots, k_scr, v_scr, L.row_cap, d->kv_heads * d->head_dim, d->batch,
+                 err_word(ws, L)};
+    return from_cuda(launch_gather(a, s));
+}
+
+qsa_status do_attend(const qsa_dims *d, const float *q, const float *k_scr, const float *v_scr,
+                     const int32_t *n_ids, float *out, void *ws, const Layout &L, cudaStream_t s)
+{
+    if (d->batch == 0) return QSA_OK;
+    AttendArgs a{q, k_scr, v_scr, n_ids, out,
+                 ws_at<float>(ws, L.off_part_m), ws_at<float>(ws, L.off_part_l),
+                 ws_at<float>(ws, L.off_part_acc), ws_at<uint32_t>(ws, L.off_tickets),
+                 L.row_cap, L.nchunk_max, d->batch, d->q_heads, d->kv_heads, d->head_dim,
+                 d->scale, err_word(ws, L)};
+    return from_cuda(launch_attend(a, s));
+}
+
+qsa_status check_shapes(const qsa_dims *d, bool score, bool attend)
+{
+    if (score && !score_shape_supported(d->idx_heads, d->idx_dim)) return QSA_ERR_UNSUPPORTED_SHAPE;
+    if (attend && !attend_shape_supported(d->head_dim, d->q_heads, d->kv_heads))
+        return QSA_ERR_UNSUPPORTED_SHAPE;
+    return QSA_OK;
+}
+
+}  // namespace
+}  // namespace qsa
+
+using namespace qsa;
+
+extern "C" {
+
+size_t qsa_workspace_size(const qsa_dims *dims)
+{
+    if (!dims_valid(dims)) return 0;
+    return make_layout(dims).total;
+}
+
+int64_t qsa_score_stride(const qsa_dims *dims)
+{
+    if (!dims_valid(dims)) return 0;
+    return make_layout(dims).score_stride;
+}
+
+int32_t qsa_row_capacity(const qsa_dims *dims)
+{
+    if (!dims_valid(dims)) return 0;
+    return make_layout(dims).row_cap;
+}
+
+qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_stats *out)
+{
+    if (!dims_valid(dims) || !out || (dims->batch > 0 && !visible_host)) return QSA_ERR_INVALID_ARG;
+    qsa_stats st;
+    std::memset(&st, 0, sizeof st);
+    for (int32_t b = 0; b < dims->batch; ++b) {
+        const int64_t T = visible_host[b];
+        if (T < 0 || T > dims->max_visible) return QSA_ERR_INVALID_ARG;
+        const int64_t G = T / kGroup;
+        const int64_t k = G < dims->budget_groups ? G : dims->budget_groups;
+        const int64_t W = kGroup * k + T % kGroup;
+        st.candidate_groups += G;
+        st.selected_groups += k;
+        st.selected_tokens += W;
+        st.raw_key_bytes += T * dims->idx_dim * 4;
+        st.kv_bytes += W * int64_t(dims->kv_heads) * dims->head_dim * 4 * 2;
+    }
+    st.pooled_key_bytes = 0;
+    st.workspace_bytes = int64_t(make_layout(dims).total);
+    st.total_bytes = st.raw_key_bytes + st.kv_bytes + st.pooled_key_bytes + st.workspace_bytes;
+    st.dense_mask_bytes = 0;  // no query-by-key mask exists anywhere in this library
+    *out = st;
+    return QSA_OK;
+}
+
+const char *qsa_status_string(qsa_status status)
+{
+    switch (status) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, or bad value)";
+    case QSA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (no kernel built for these dimensions)";
+    case QSA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than qsa_workspace_size(dims)";
+    case QSA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case QSA_ERR_DEVICE_FAULT: return "the device error word was set (see QSA_DEVERR_* bits)";
+    }
+    return "unknown status";
+}
+
+qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    if (!ws || !aligned(ws, kWsAlign)) return QSA_ERR_INVALID_ARG;
+    if (ws_bytes == 0) return QSA_OK;
+    return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_check_errors(void *ws, size_t ws_bytes, void *stream, uint32_t *flags_out)
+{
+    if (!ws || !aligned(ws, kWsAlign) || ws_bytes < kWsAlign) return QSA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t flags = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QSA_ERR_CUDA;
+    if (cudaMemcpy(&flags, ws, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return QSA_ERR_CUDA;
+    if (flags != 0 && cudaMemset(ws, 0, sizeof flags) != cudaSuccess) return QSA_ERR_CUDA;
+    if (flags_out) *flags_out = flags;
+    return flags ? QSA_ERR_DEVICE_FAULT : QSA_OK;
+}
+
+qsa_status qsa_score_groups(const qsa_dims *dims, const qsa_inputs *in, float *scores, void *ws,
+                            size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, true, false)) != QSA_OK) return st;
+    if ((st = check_inputs_score(in)) != QSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_score(dims, in, scores, L.score_stride, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_select(const qsa_dims *dims, const int32_t *visible, const float *scores, int32_t *ids,
+                      int32_t *n_ids, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    if (!visible || !scores || !ids || !n_ids) return QSA_ERR_INVALID_ARG;
+    if (!aligned(visible, 4) || !aligned(scores, 16) || !aligned(ids, 4) || !aligned(n_ids, 4))
+        return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_select(dims, visible, scores, L.score_stride, ids, n_ids, ws, L,
+                     static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
+                      float *k_scr, float *v_scr, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_inputs_gather(in)) != QSA_OK) return st;
+    if (!ids || !n_ids || !k_scr || !v_scr) return QSA_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(k_scr, 16) || !aligned(v_scr, 16))
+        return QSA_ERR_INVALID_ARG;
+    if ((dims->kv_heads * dims->head_dim) % 4 != 0) return QSA_ERR_UNSUPPORTED_SHAPE;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_gather(dims, in, ids, n_ids, k_scr, v_scr, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr, const float *v_scr,
+                      const int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, false, true)) != QSA_OK) return st;
+    if (!q || !k_scr || !v_scr || !n_ids || !out) return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_scr, 16) || !aligned(v_scr, 16) || !aligned(n_ids, 4) ||
+        !aligned(out, 4))
+        return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_attend(dims, q, k_scr, v_scr, n_ids, out, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids, float *out,
+                      void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, true, true)) != QSA_OK) return st;
+    if ((st = check_inputs_score(in)) != QSA_OK) return st;
+    if ((st = check_inputs_gather(in)) != QSA_OK) return st;
+    if (!in->q || !aligned(in->q, 16)) return QSA_ERR_INVALID_ARG;
+    if (!ids || !n_ids || !out || !aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(out, 4))
+        return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float *scores = ws_at<float>(ws, L.off_scores);
+    float *k_scr = ws_at<float>(ws, L.off_kscr);
+    float *v_scr = ws_at<float>(ws, L.off_vscr);
+    if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s)) != QSA_OK) return st;
+    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s)) != QSA_OK) return st;
+    if ((st = do_gather(dims, in, ids, n_ids, k_scr, v_scr, ws, L, s)) != QSA_OK) return st;
+    return do_attend(dims, in->q, k_scr, v_scr, n_ids, out, ws, L, s);
+}
+
+}  // extern "C"

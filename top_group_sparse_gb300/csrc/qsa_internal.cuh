@@ -1,0 +1,169 @@
+// qsa_internal.cuh -- internal declarations and device helpers of libqsa.
+//
+// Everything here is private to the library: the public boundary is
+// include/qsa.h.  Kernels never trap: a bad index is skipped and recorded in
+// the sticky device error word; every wait on an mbarrier is bounded in time.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qsa.h"
+
+namespace qsa {
+
+// ---- workspace layout -----------------------------------------------------
+
+constexpr int kGroup = 4;            // tokens per scored group
+constexpr int kAttendChunk = 64;     // rows per attention chunk (fixed: the split
+                                     // depends on the row length only)
+constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+    int64_t score_stride;   // floats per scores row
+    int32_t row_cap;        // IDs per row: 4*budget + 3
+    int32_t nchunk_max;     // attention chunks per row at full capacity
+    size_t off_err, off_tickets, off_part_m, off_part_l, off_part_acc;
+    size_t off_scores, off_kscr, off_vscr;
+    size_t total;
+};
+
+bool dims_valid(const qsa_dims *d);
+Layout make_layout(const qsa_dims *d);
+
+// ---- launchers (one per stage) --------------------------------------------
+
+struct ScoreArgs {
+    const float *q_idx;
+    const float *idx_keys;
+    const int64_t *key_offset;
+    const int32_t *visible;
+    float *scores;
+    int64_t score_stride;
+    int32_t batch, idx_heads, idx_dim, max_visible;
+    uint32_t *err;
+};
+bool score_shape_supported(int idx_heads, int idx_dim);
+cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
+
+struct SelectArgs {
+    const int32_t *visible;
+    const float *scores;
+    int64_t score_stride;
+    int32_t *ids;
+    int32_t *n_ids;
+    int32_t row_cap, budget, max_visible, batch;
+    uint32_t *err;
+};
+cudaError_t launch_select(const SelectArgs &a, cudaStream_t s);
+
+struct GatherArgs {
+    const int32_t *visible;
+    const int32_t *ids;
+    const int32_t *n_ids;
+    const int32_t *slot_map;
+    const int64_t *slot_offset;
+    const float *k_cache, *v_cache;
+    int64_t num_slots;
+    float *k_scr, *v_scr;
+    int32_t row_cap, row_floats, batch;
+    uint32_t *err;
+};
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
+
+struct AttendArgs {
+    const float *q;
+    const float *k_scr, *v_scr;
+    const int32_t *n_ids;
+    float *out;
+    float *part_m, *part_l, *part_acc;
+    uint32_t *tickets;
+    int32_t row_cap, nchunk_max, batch, q_heads, kv_heads, head_dim;
+    float scale;
+    uint32_t *err;
+};
+bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
+cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s);
+
+// ---- device helpers ---------------------------------------------------------
+
+__device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit)
+{
+    atomicOr(err, bit);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    // make the initialised barriers visible to the async (bulk copy) proxy
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the given phase parity of an mbarrier for at most limit_ns
+// nanoseconds of wall time.  Returns false if the time ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// One-dimensional bulk copy global -> shared, completing on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;     // 1 s for a copy to land
+constexpr uint64_t kDrainLimitNs = 100000000ull;     // 0.1 s per copy when draining
+
+}  // namespace qsa

@@ -1,0 +1,306 @@
+"""Thin ctypes binding of libqsa (``include/qsa.h``) -- argument marshalling only.
+
+Every function carries the name of the C entry point it calls and does
+nothing but turn torch tensors (device memory) and plain Python values into
+the C arguments; every step of the path runs in the library's CUDA kernels.
+The library is loaded on first use; if it is missing or fails to load, the
+call raises -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
+    "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
+    "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode", "make_dims", "DeviceBatch",
+    "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
+    "QSA_DEVERR_WAIT_TIMEOUT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libqsa.so")
+
+QSA_OK = 0
+QSA_ERR_DEVICE_FAULT = 5
+QSA_DEVERR_VISIBLE_RANGE = 0x1
+QSA_DEVERR_SLOT_RANGE = 0x2
+QSA_DEVERR_ROW_RANGE = 0x4
+QSA_DEVERR_WAIT_TIMEOUT = 0x8
+
+
+class QsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status}: {msg}")
+        self.status = status
+
+
+class QsaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("idx_heads", ctypes.c_int32),
+                ("idx_dim", ctypes.c_int32), ("q_heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("budget_groups", ctypes.c_int32),
+                ("max_visible", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+class QsaInputs(ctypes.Structure):
+    _fields_ = [("q_idx", ctypes.c_void_p), ("idx_keys", ctypes.c_void_p),
+                ("key_offset", ctypes.c_void_p), ("visible", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("slot_map", ctypes.c_void_p), ("slot_offset", ctypes.c_void_p)]
+
+
+class QsaStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "candidate_groups", "selected_groups", "selected_tokens", "raw_key_bytes", "kv_bytes",
+        "pooled_key_bytes", "workspace_bytes", "total_bytes", "dense_mask_bytes")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+_lib = None
+_P = ctypes.c_void_p
+_DP = ctypes.POINTER(QsaDims)
+_IP = ctypes.POINTER(QsaInputs)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libqsa.so (raises if it is not built or cannot be loaded)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libqsa.so is not built ({p}); run __graft_entry__.build() first")
+    L = ctypes.CDLL(p)
+    L.qsa_workspace_size.argtypes = [_DP]
+    L.qsa_workspace_size.restype = ctypes.c_size_t
+    L.qsa_score_stride.argtypes = [_DP]
+    L.qsa_score_stride.restype = ctypes.c_int64
+    L.qsa_row_capacity.argtypes = [_DP]
+    L.qsa_row_capacity.restype = ctypes.c_int32
+    L.qsa_get_stats.argtypes = [_DP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(QsaStats)]
+    L.qsa_get_stats.restype = ctypes.c_int
+    L.qsa_status_string.argtypes = [ctypes.c_int]
+    L.qsa_status_string.restype = ctypes.c_char_p
+    L.qsa_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
+    L.qsa_workspace_init.restype = ctypes.c_int
+    L.qsa_check_errors.argtypes = [_P, ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_uint32)]
+    L.qsa_check_errors.restype = ctypes.c_int
+    L.qsa_score_groups.argtypes = [_DP, _IP, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_score_groups.restype = ctypes.c_int
+    L.qsa_select.argtypes = [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_select.restype = ctypes.c_int
+    L.qsa_gather.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_gather.restype = ctypes.c_int
+    L.qsa_attend.argtypes = [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_attend.restype = ctypes.c_int
+    L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_decode.restype = ctypes.c_int
+    if path is None:
+        _lib = L
+    return L
+
+
+def exported_symbols(header: str | None = None) -> list[str]:
+    """Names of the functions include/qsa.h declares."""
+    import re
+    header = header or os.path.join(os.path.dirname(_PKG), "include", "qsa.h")
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_]+)\s*\(", text)))
+
+
+# ---- marshalling helpers ----------------------------------------------------
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _ws(ws):
+    """(pointer, bytes) of a workspace given as a tensor or a (ptr, bytes) pair."""
+    if isinstance(ws, tuple):
+        return ws
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def _check(fn: str, st: int):
+    if st != QSA_OK:
+        raise QsaError(fn, st, load().qsa_status_string(st).decode())
+    return st
+
+
+def make_dims(batch, idx_heads, idx_dim, q_heads, kv_heads, head_dim, budget_groups=512,
+              max_visible=0, scale=None, group=4) -> QsaDims:
+    if scale is None:
+        scale = float(np.float32(1.0 / np.sqrt(head_dim)))
+    return QsaDims(int(batch), int(idx_heads), int(idx_dim), int(q_heads), int(kv_heads),
+                   int(head_dim), int(group), int(budget_groups), int(max_visible), float(scale))
+
+
+# ---- the C entry points -----------------------------------------------------
+
+def qsa_workspace_size(dims: QsaDims) -> int:
+    return int(load().qsa_workspace_size(ctypes.byref(dims)))
+
+
+def qsa_score_stride(dims: QsaDims) -> int:
+    return int(load().qsa_score_stride(ctypes.byref(dims)))
+
+
+def qsa_row_capacity(dims: QsaDims) -> int:
+    return int(load().qsa_row_capacity(ctypes.byref(dims)))
+
+
+def qsa_get_stats(dims: QsaDims, visible_host) -> dict:
+    vis = np.ascontiguousarray(np.asarray(visible_host, dtype=np.int32))
+    st = QsaStats()
+    _check("qsa_get_stats", load().qsa_get_stats(
+        ctypes.byref(dims), vis.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(st)))
+    return st.as_dict()
+
+
+def qsa_status_string(status: int) -> str:
+    return load().qsa_status_string(int(status)).decode()
+
+
+def qsa_workspace_init(ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_workspace_init", load().qsa_workspace_init(p, n, _stream(stream)))
+
+
+def qsa_check_errors(ws, stream=None) -> tuple[int, int]:
+    """Returns (status, flags); does not raise on QSA_ERR_DEVICE_FAULT."""
+    p, n = _ws(ws)
+    flags = ctypes.c_uint32(0)
+    st = load().qsa_check_errors(p, n, _stream(stream), ctypes.byref(flags))
+    if st not in (QSA_OK, QSA_ERR_DEVICE_FAULT):
+        _check("qsa_check_errors", st)
+    return int(st), int(flags.value)
+
+
+def qsa_score_groups(dims, inputs, scores, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_score_groups", load().qsa_score_groups(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(scores), p, n, _stream(stream)))
+
+
+def qsa_select(dims, visible, scores, ids, n_ids, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_select", load().qsa_select(
+        ctypes.byref(dims), _ptr(visible), _ptr(scores), _ptr(ids), _ptr(n_ids), p, n,
+        _stream(stream)))
+
+
+def qsa_gather(dims, inputs, ids, n_ids, k_scr, v_scr, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_gather", load().qsa_gather(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(k_scr),
+        _ptr(v_scr), p, n, _stream(stream)))
+
+
+def qsa_attend(dims, q, k_scr, v_scr, n_ids, out, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_attend", load().qsa_attend(
+        ctypes.byref(dims), _ptr(q), _ptr(k_scr), _ptr(v_scr), _ptr(n_ids), _ptr(out), p, n,
+        _stream(stream)))
+
+
+def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_decode", load().qsa_decode(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(out), p, n,
+        _stream(stream)))
+
+
+# ---- device-resident batch (plumbing: torch owns the memory) ----------------
+
+class DeviceBatch:
+    """The arrays of one workload copied into device memory, with the output
+    buffers and the workspace the library needs, all allocated by torch."""
+
+    def __init__(self, w, device="cuda", budget=None, queries=None):
+        import torch
+        self.w = w
+        sel = np.arange(w.batch) if queries is None else np.asarray(queries, np.int64)
+        dev = torch.device(device)
+
+        def put(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        self.q_idx = put(w.q_idx[sel])
+        self.idx_keys = put(w.idx_keys)
+        self.key_offset = put(w.key_offset[sel])
+        self.visible = put(w.visible[sel])
+        self.q = put(w.q[sel])
+        self.k_cache = put(w.k_cache)
+        self.v_cache = put(w.v_cache)
+        self.slot_map = put(w.slot_map)
+        self.slot_offset = put(w.slot_offset[sel])
+        B = len(sel)
+        mv = int(w.visible[sel].max(initial=0))
+        self.dims = make_dims(B, w.idx_heads, w.idx_dim, w.q_heads, w.kv_heads, w.head_dim,
+                              budget_groups=w.budget if budget is None else budget,
+                              max_visible=max(mv, w.max_visible if queries is None else mv),
+                              scale=w.scale)
+        self.inputs = QsaInputs(
+            _ptr(self.q_idx), _ptr(self.idx_keys), _ptr(self.key_offset), _ptr(self.visible),
+            _ptr(self.q), _ptr(self.k_cache), _ptr(self.v_cache), int(w.num_slots),
+            _ptr(self.slot_map), _ptr(self.slot_offset))
+        self.row_cap = qsa_row_capacity(self.dims)
+        self.score_stride = qsa_score_stride(self.dims)
+        nbytes = qsa_workspace_size(self.dims)
+        if nbytes == 0:
+            raise ValueError("invalid dims")
+        # zero-filled: the workspace header must start clean
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        self.ids = torch.full((B, self.row_cap), -1, dtype=torch.int32, device=dev)
+        self.n_ids = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        self.out = torch.full((B, w.q_heads, w.head_dim), float("nan"), dtype=torch.float32, device=dev)
+        self.scores = torch.full((B, self.score_stride), float("nan"), dtype=torch.float32, device=dev)
+        self.k_scr = torch.zeros((B, self.row_cap, w.kv_heads, w.head_dim), dtype=torch.float32, device=dev)
+        self.v_scr = torch.zeros_like(self.k_scr)
+
+    # the four stages and the whole path, on this batch's buffers
+    def score(self, stream=None):
+        return qsa_score_groups(self.dims, self.inputs, self.scores, self.ws, stream)
+
+    def select(self, stream=None):
+        return qsa_select(self.dims, self.visible, self.scores, self.ids, self.n_ids, self.ws, stream)
+
+    def gather(self, stream=None):
+        return qsa_gather(self.dims, self.inputs, self.ids, self.n_ids, self.k_scr, self.v_scr,
+                          self.ws, stream)
+
+    def attend(self, stream=None):
+        return qsa_attend(self.dims, self.q, self.k_scr, self.v_scr, self.n_ids, self.out,
+                          self.ws, stream)
+
+    def decode(self, stream=None):
+        return qsa_decode(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws, stream)
+
+    def check_errors(self, stream=None):
+        return qsa_check_errors(self.ws, stream)
