@@ -161,7 +161,7 @@ def run_reference(args):
         return 0
     import oracle
     from top_group_sparse_gb300 import workloads as wl
-    w = wl.long_262144()
+    w = wl.long_262144(batch=args.batch)
     t0 = time.perf_counter()
     oracle.decode(w, queries=[0])
     per_query = time.perf_counter() - t0
@@ -211,7 +211,7 @@ def run_gpu(args):
     build.build()
     qsa.load()
 
-    w = wl.long_262144(seed=4 + 1000 * rank)
+    w = wl.long_262144(seed=4 + 1000 * rank, batch=args.batch)
     db = qsa.DeviceBatch(w, device=f"cuda:{local}")
     stream = torch.cuda.current_stream()
 
@@ -389,6 +389,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--batch", type=int, default=8,
+                    help="queries per GPU (8 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
