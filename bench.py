@@ -208,6 +208,7 @@ def run_gpu(args):
 
     from top_group_sparse_gb300 import build, qsa
     from top_group_sparse_gb300 import workloads as wl
+    from top_group_sparse_gb300.sharding import max_over_ranks
     build.build()
     qsa.load()
 
@@ -274,11 +275,7 @@ def run_gpu(args):
 
     step_ms = np.array([e[0].elapsed_time(e[4]) for e in events])
     stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in events])
-    total_ms = float(step_ms.sum())
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=db.out.device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), db.out.device)
     ms_per_step = total_ms / K
     value = ws * w.batch * K / (total_ms / 1e3)
 
@@ -313,11 +310,7 @@ def run_gpu(args):
     t0 = time.perf_counter()
     for _ in range(K2):
         e2e_step()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=db.out.device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, db.out.device)
     e2e_value = ws * w.batch * K2 / e2e_s
 
     if rank != 0:
