@@ -207,6 +207,34 @@ qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr,
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 
+/* ---- attention without a workspace -------------------------------------- */
+
+/* Fixed size of the device scratch behind qsa_attend_noalloc (4 MiB); every
+ * GPU that loads the library holds it until the process exits. */
+#define QSA_ATTEND_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* Stage 4 without a workspace.  The notes have no counterpart to this call:
+ * it exists for callers that cannot allocate device memory or pass a
+ * workspace -- e.g. a plugin whose host runtime owns all device memory and
+ * forbids third-party allocations, or a loop that must not allocate once it
+ * runs.  Same arguments, kernel and results as qsa_attend, minus `ws`: the
+ * error word, merge tickets and chunk partials live in one static device
+ * array of QSA_ATTEND_NOALLOC_SCRATCH_BYTES.  Nothing is allocated or freed.
+ *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*C*4)
+ *    + align256(B*n_q*C*d*4) bytes must fit, C = ceil((4*budget+3)/64);
+ *    larger dims return QSA_ERR_WORKSPACE_TOO_SMALL before anything is
+ *    enqueued (e.g. B=8, n_q=16, d=128, budget 512 needs 2.2 MB: fits).
+ *  - The first call on each device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *    first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents: each
+ *    call clears the error word and tickets on `stream` first.  Calls that
+ *    overlap on the GPU (other streams, other threads) race on it.
+ *  - Device-detected errors (an n_ids[b] outside [0, 4*budget+3]) zero that
+ *    query's output; the error word is not reported by this call. */
+qsa_status qsa_attend_noalloc(const qsa_dims *dims, const float *q, const float *k_scr,
+                              const float *v_scr, const int32_t *n_ids, float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

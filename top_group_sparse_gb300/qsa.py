@@ -17,7 +17,8 @@ __all__ = [
     "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
     "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
-    "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode", "make_dims", "DeviceBatch",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode", "qsa_attend_noalloc", "make_dims",
+    "DeviceBatch",
     "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
     "QSA_DEVERR_WAIT_TIMEOUT",
 ]
@@ -107,6 +108,8 @@ def load(path: str | None = None):
     L.qsa_attend.restype = ctypes.c_int
     L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode.restype = ctypes.c_int
+    L.qsa_attend_noalloc.argtypes = [_DP, _P, _P, _P, _P, _P, _P]
+    L.qsa_attend_noalloc.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -233,6 +236,14 @@ def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
     p, n = _ws(ws)
     return _check("qsa_decode", load().qsa_decode(
         ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(out), p, n,
+        _stream(stream)))
+
+
+def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
+    """Attention stage with the library's fixed static scratch instead of a
+    workspace, for callers that cannot allocate device memory."""
+    return _check("qsa_attend_noalloc", load().qsa_attend_noalloc(
+        ctypes.byref(dims), _ptr(q), _ptr(k_scr), _ptr(v_scr), _ptr(n_ids), _ptr(out),
         _stream(stream)))
 
 
