@@ -7,13 +7,14 @@ groups, indexer 8 heads x 64, GQA attention 16 query / 2 KV heads x 128, all
 values N(0,1), K/V in a wrapped ring buffer (slot = (t + 131,072) mod
 262,144).  One step = one pass of the whole hot path over the batch: group
 scoring, set choice + chronological emission, slot resolution + compact
-gather, online-softmax attention -- the four C-ABI stage calls that
-qsa_decode issues, with a CUDA event between stages.
+gather, online-softmax attention -- the three C-ABI stage calls that
+qsa_decode issues (scoring, selection, fused gather + attention), with a
+CUDA event between stages.
 
 Timing: W untimed warm-up steps, then K timed steps.  Before each timed step
 L2 is flushed (a 256 MiB buffer written, then another 256 MiB read), outside
 the events; the step time is the device time between the events around its
-four launches.  Under torchrun every rank runs its own batch (weak scaling,
+three launches.  Under torchrun every rank runs its own batch (weak scaling,
 no collective on the data path) and the slowest rank's time counts.
 
 Prints one JSON line.  --impl reference times the CPU oracle instead.
@@ -242,14 +243,14 @@ def run_gpu(args):
         torch.sum(flush_r, dim=0, out=sink[0])
 
     def step(ev=None):
+        # exactly the launches of qsa_decode, one C-ABI stage call each
         if ev is None:
-            db.score(stream); db.select(stream); db.gather(stream); db.attend(stream)
+            db.score(stream); db.select(stream); db.gather_attend(stream)
             return
         ev[0].record(stream); db.score(stream)
         ev[1].record(stream); db.select(stream)
-        ev[2].record(stream); db.gather(stream)
-        ev[3].record(stream); db.attend(stream)
-        ev[4].record(stream)
+        ev[2].record(stream); db.gather_attend(stream)
+        ev[3].record(stream)
 
     for _ in range(args.warmup):
         flush()
@@ -257,7 +258,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier()
@@ -273,8 +274,8 @@ def run_gpu(args):
     if st != 0:
         raise SystemExit(f"device error word {flags:#x} after the timed loop")
 
-    step_ms = np.array([e[0].elapsed_time(e[4]) for e in events])
-    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in events])
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in events])
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in events])
     total_ms = max_over_ranks(float(step_ms.sum()), db.out.device)
     ms_per_step = total_ms / K
     value = ws * w.batch * K / (total_ms / 1e3)
@@ -354,7 +355,7 @@ def run_gpu(args):
                 "note": "qsa_decode per step; queries copied in from pinned host memory, ID rows "
                         "and outputs copied back, stream synchronised; K/V cache and index-key "
                         "history resident in HBM"},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 3 * K,
         "roofline": {"kernel": "score_groups", "bound": "hbm", "achieved": score_gbs,
                      "peak": peak, "unit": "GB/s", "frac": score_gbs / peak,
                      "traffic": profile_traffic(),
@@ -363,7 +364,7 @@ def run_gpu(args):
         "path_hbm": {"achieved_gbs": path_gbs, "frac_of_measured": path_gbs / peak,
                      "frac_of_8tbs": path_gbs / 8000.0, "algorithmic_bytes_per_step": path_bytes},
         "stages_us": {n: float(v * 1e3) for n, v in
-                      zip(("score", "select", "gather", "attend"), stage_mean)},
+                      zip(("score", "select", "gather_attend"), stage_mean)},
         "loop_wall_s": loop_wall,
         "parity_sample": parity,
     }

@@ -201,9 +201,19 @@ qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr,
                       const float *v_scr, const int32_t *n_ids, float *out,
                       void *ws, size_t ws_bytes, void *stream);
 
-/* The whole path -- stages 1-4 back to back on `stream`, with scores and K/V
- * scratch kept in the workspace.  Outputs: ids, n_ids (as qsa_select) and
- * out (as qsa_attend). */
+/* Stages 3 and 4 in one launch: each attention CTA resolves its rows'
+ * slots, copies exactly those K/V rows from the cache, writes them to
+ * k_scr / v_scr (the same bytes as qsa_gather) and runs the attention of
+ * qsa_attend on them from on-chip memory.  Outputs: k_scr, v_scr (as
+ * qsa_gather) and out (as qsa_attend), bit-identical to qsa_gather followed
+ * by qsa_attend. */
+qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids,
+                             const int32_t *n_ids, float *k_scr, float *v_scr, float *out,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* The whole path on `stream`: qsa_score_groups, qsa_select and
+ * qsa_gather_attend back to back, with scores and K/V scratch kept in the
+ * workspace.  Outputs: ids, n_ids (as qsa_select) and out (as qsa_attend). */
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 

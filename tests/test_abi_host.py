@@ -20,10 +20,11 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 13
+    assert len(names) == 14
     for n in names:
         assert hasattr(lib, n), n
-    for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode"):
+    for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",
+              "qsa_decode"):
         assert n in names
 
 

@@ -125,7 +125,7 @@ def test_heavy_ties_on_integer_grid_long():
 
 def test_select_uncached_long_history():
     """A history long enough that a cluster slice of scores no longer fits in
-    shared memory (G > 8 * 49152), so select streams scores from global."""
+    shared memory (G > 8 * 24576), so select streams scores from global."""
     T = 8 * 49152 * 4 + 4 * 1000 + 2
     w = wl.make_workload("long", [T], idx_heads=4, idx_dim=32, q_heads=2, kv_heads=2,
                          head_dim=64, seed=13, slots="ring", ring_size=T, ring_shift=777)
@@ -180,3 +180,31 @@ def test_stats_report_zero_dense_mask():
     st = qsa.qsa_get_stats(db.dims, w.visible)
     assert st["dense_mask_bytes"] == 0
     assert st["selected_tokens"] == 37 and st["candidate_groups"] == 9
+
+
+@pytest.mark.parametrize("shape", [(16, 2, 128), (4, 4, 64), (12, 1, 64), (3, 3, 128)])
+def test_gather_attend_equals_gather_then_attend(shape):
+    """The fused stage writes the same scratch bytes as qsa_gather and the same
+    output bits as qsa_attend on that scratch, for GQA ratios 8, 1, 12, 1."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    nq, nkv, hd = shape
+    w = wl.make_workload("ga", [9001, 2052, 0, 3, 40000, 2051, 65], idx_heads=8, idx_dim=64,
+                         q_heads=nq, kv_heads=nkv, head_dim=hd, seed=55 + nq, slots="paged16")
+    db = qsa.DeviceBatch(w)
+    db.score(); db.select(); db.gather(); db.attend()
+    torch.cuda.synchronize()
+    k1, v1, o1 = db.k_scr.clone(), db.v_scr.clone(), db.out.clone()
+    db.k_scr.zero_(); db.v_scr.zero_(); db.out.fill_(float("nan"))
+    db.gather_attend()
+    st, flags = db.check_errors()
+    assert st == 0, f"device error word {flags:#x}"
+    n = db.n_ids.cpu().numpy()
+    for b in range(w.batch):
+        assert torch.equal(db.k_scr[b, :n[b]], k1[b, :n[b]])
+        assert torch.equal(db.v_scr[b, :n[b]], v1[b, :n[b]])
+    assert torch.equal(db.out, o1)
+    ref = oracle_run(w)
+    gpu = {"ids": db.ids.cpu().numpy(), "n_ids": n, "out": db.out.cpu().numpy()}
+    assert_ids_equal(w, gpu, ref)
+    assert_attention_close(w, gpu, ref)

@@ -158,6 +158,20 @@ qsa_status do_attend(const qsa_dims *d, const float *q, const float *k_scr, cons
     return from_cuda(launch_attend(a, s));
 }
 
+qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
+                            float *k_scr, float *v_scr, float *out, void *ws, const Layout &L, cudaStream_t s)
+{
+    if (d->batch == 0) return QSA_OK;
+    AttendArgs a{in->q, nullptr, nullptr, n_ids, out,
+                 ws_at<float>(ws, L.off_part_m), ws_at<float>(ws, L.off_part_l),
+                 ws_at<float>(ws, L.off_part_acc), ws_at<uint32_t>(ws, L.off_tickets),
+                 L.row_cap, L.nchunk_max, d->batch, d->q_heads, d->kv_heads, d->head_dim,
+                 d->scale, err_word(ws, L),
+                 ids, in->visible, in->slot_map, in->slot_offset, in->k_cache, in->v_cache, in->num_slots,
+                 k_scr, v_scr};
+    return from_cuda(launch_attend(a, s));
+}
+
 qsa_status check_shapes(const qsa_dims *d, bool score, bool attend)
 {
     if (score && !score_shape_supported(d->idx_heads, d->idx_dim)) return QSA_ERR_UNSUPPORTED_SHAPE;
@@ -298,11 +312,27 @@ qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr, 
     if ((st = check_shapes(dims, false, true)) != QSA_OK) return st;
     if (!q || !k_scr || !v_scr || !n_ids || !out) return QSA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_scr, 16) || !aligned(v_scr, 16) || !aligned(n_ids, 4) ||
-        !aligned(out, 4))
+        !aligned(out, 16))
         return QSA_ERR_INVALID_ARG;
     if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
     const Layout L = make_layout(dims);
     return do_attend(dims, q, k_scr, v_scr, n_ids, out, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
+                             float *k_scr, float *v_scr, float *out, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, false, true)) != QSA_OK) return st;
+    if ((st = check_inputs_gather(in)) != QSA_OK) return st;
+    if (!in->q || !aligned(in->q, 16)) return QSA_ERR_INVALID_ARG;
+    if (!ids || !n_ids || !k_scr || !v_scr || !out) return QSA_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(k_scr, 16) || !aligned(v_scr, 16) || !aligned(out, 16))
+        return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, static_cast<cudaStream_t>(stream));
 }
 
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids, float *out,
@@ -314,7 +344,7 @@ qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, 
     if ((st = check_inputs_score(in)) != QSA_OK) return st;
     if ((st = check_inputs_gather(in)) != QSA_OK) return st;
     if (!in->q || !aligned(in->q, 16)) return QSA_ERR_INVALID_ARG;
-    if (!ids || !n_ids || !out || !aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(out, 4))
+    if (!ids || !n_ids || !out || !aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(out, 16))
         return QSA_ERR_INVALID_ARG;
     if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
     const Layout L = make_layout(dims);
@@ -324,8 +354,7 @@ qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, 
     float *v_scr = ws_at<float>(ws, L.off_vscr);
     if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s)) != QSA_OK) return st;
     if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s)) != QSA_OK) return st;
-    if ((st = do_gather(dims, in, ids, n_ids, k_scr, v_scr, ws, L, s)) != QSA_OK) return st;
-    return do_attend(dims, in->q, k_scr, v_scr, n_ids, out, ws, L, s);
+    return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, s);
 }
 
 }  // extern "C"

@@ -92,7 +92,7 @@ extern "C" qsa_status qsa_attend_noalloc(const qsa_dims *dims, const float *q, c
     const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_scr) |
                           reinterpret_cast<uintptr_t>(v_scr);
     if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(n_ids) & 3u) != 0 ||
-        (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+        (reinterpret_cast<uintptr_t>(out) & 15u) != 0)
         return QSA_ERR_INVALID_ARG;
     const Layout W = make_layout(dims);  // row capacity and chunk count, as qsa_attend
     const StaticLayout L = static_layout(dims, W.nchunk_max);

@@ -76,7 +76,7 @@ cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
 
 struct AttendArgs {
     const float *q;
-    const float *k_scr, *v_scr;
+    const float *k_scr, *v_scr;      // rows read from the gathered scratch (k_cache == nullptr)
     const int32_t *n_ids;
     float *out;
     float *part_m, *part_l, *part_acc;
@@ -84,6 +84,15 @@ struct AttendArgs {
     int32_t row_cap, nchunk_max, batch, q_heads, kv_heads, head_dim;
     float scale;
     uint32_t *err;
+    // fused gather: when k_cache != nullptr, rows are resolved through the slot
+    // map, copied from the cache, and also written to k_scr_out / v_scr_out
+    const int32_t *ids;
+    const int32_t *visible;
+    const int32_t *slot_map;
+    const int64_t *slot_offset;
+    const float *k_cache, *v_cache;
+    int64_t num_slots;
+    float *k_scr_out, *v_scr_out;
 };
 bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s);

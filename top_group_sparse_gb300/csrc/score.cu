@@ -14,14 +14,14 @@
 // implementation of that order.  No tensor cores: the order is the contract.
 //
 // The stage is a stream over the raw keys (T * D * 4 bytes per query), so it
-// is bound by HBM bandwidth.  Design: one persistent CTA per SM walks tiles
-// (TG groups of one query, contiguous in memory) with a ring of kStages
-// shared-memory buffers filled by one-dimensional bulk copies
-// (cp.async.bulk + mbarrier complete_tx), so ~160 KB per SM is in flight.
-// Each tile is pooled cooperatively into shared memory (coalesced, conflict
-// free), then thread (g, h) runs the D-long FMA chain of head h for group g
-// with q_h in registers, and the H head results are summed in order through
-// warp shuffles.
+// is bound by HBM bandwidth.  Design: persistent CTAs (two per SM for the
+// usual shapes) walk tiles -- TG groups of one query, one contiguous block --
+// with a ring of shared-memory stages filled by one-dimensional bulk copies
+// (cp.async.bulk + mbarrier complete_tx), ~192 KB in flight per SM.  Each
+// tile is pooled cooperatively, 16 bytes per thread-item, into a swizzled
+// double-buffered pooled tile (one barrier per tile); then thread (g, h) runs
+// the D-long FMA chain of head h for group g with q_h in registers, and the H
+// head results are summed in order after a warp shuffle gather.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -34,37 +34,59 @@ struct ScoreCfg {
     static constexpr int kGroupFloats = kGroup * D;         // raw floats per group
     static constexpr int kStageFloats = kTG * kGroupFloats;
     static constexpr int kStageBytes = kStageFloats * 4;
-    static constexpr int kStagesRaw = 163840 / kStageBytes;
+    // Two CTAs per SM when a stage is small enough, so that one CTA's
+    // barriers and FMA chains overlap the other's; ~96-192 KB of raw keys in
+    // flight per SM either way.
+    static constexpr int kCtasPerSm = kStageBytes <= 32768 ? 2 : 1;
+    static constexpr int kStageBudget = kCtasPerSm == 2 ? 98304 : 196608;
+    static constexpr int kStagesRaw = kStageBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-    static constexpr int kPoolStride = D + 4;               // floats; keeps float4 rows
-                                                            // on distinct banks
-    static constexpr size_t kPoolBytes = size_t(kTG) * kPoolStride * 4;
-    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + kPoolBytes + kStages * 8;
+    static constexpr int kPoolFloats = kTG * D;             // one pooled tile (swizzled)
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * size_t(kPoolFloats) * 4 + kStages * 8;
     static_assert(kThreads % H == 0 && 32 % H == 0, "heads must divide a warp");
-    static_assert(D % 4 == 0, "index keys are read as float4");
+    static_assert(D % 32 == 0, "the pooled-tile swizzle needs D/4 to be a multiple of 8");
+    static_assert(kSmem <= 232448, "shared memory per CTA");
 };
+
+// Pooled tile layout: group g's 16-byte chunk j4 sits at chunk (j4 ^ (g & 7))
+// of row g, so the 4 or 8 groups a warp reads at once hit distinct banks.
+template <int D>
+__device__ __forceinline__ int pool_index(int g, int j4)
+{
+    return g * D + ((j4 ^ (g & 7)) << 2);
+}
+
+// Per-query values a thread needs, reloaded only when the query changes.
+struct QueryCache {
+    int b = -1;
+    int G = 0;
+};
+
+__device__ __forceinline__ int groups_of(const ScoreArgs &a, int b, QueryCache &qc)
+{
+    if (b != qc.b) {
+        const int T = __ldg(a.visible + b);
+        qc.b = b;
+        qc.G = (T < 0 || T > a.max_visible) ? 0 : (T >> 2);
+    }
+    return qc.G;
+}
 
 struct TileRef {
     int b;      // query
     int g0;     // first group of the tile
-    int n;      // valid groups in the tile (0 = nothing to do)
+    int n;      // valid groups in the tile
 };
 
-__device__ __forceinline__ int groups_of(const ScoreArgs &a, int b)
-{
-    const int T = __ldg(a.visible + b);
-    return (T < 0 || T > a.max_visible) ? 0 : (T >> 2);
-}
-
-// Next tile t' >= t (stepping by `step`) that holds at least one group.
+// Next tile t' >= t (below `end`) that holds at least one group.
 template <int TG>
-__device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int step, int total,
-                                         int tiles_per_q, TileRef &ref)
+__device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int end, int tiles_per_q,
+                                         QueryCache &qc, TileRef &ref)
 {
-    for (; t < total; t += step) {
+    for (; t < end; ++t) {
         const int b = t / tiles_per_q;
         const int g0 = (t - b * tiles_per_q) * TG;
-        const int G = groups_of(a, b);
+        const int G = groups_of(a, b, qc);
         if (g0 < G) {
             ref.b = b;
             ref.g0 = g0;
@@ -72,26 +94,30 @@ __device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int step, in
             return t;
         }
     }
-    return total;
+    return end;
 }
 
 template <int H, int D>
-__global__ void __launch_bounds__(ScoreCfg<H, D>::kThreads, 1)
+__global__ void __launch_bounds__(ScoreCfg<H, D>::kThreads, ScoreCfg<H, D>::kCtasPerSm)
 score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 {
     using C = ScoreCfg<H, D>;
+    constexpr int F4 = D / 4;
     extern __shared__ __align__(128) unsigned char smem[];
     float *stages = reinterpret_cast<float *>(smem);
     float *pooled = reinterpret_cast<float *>(smem + size_t(C::kStages) * C::kStageBytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(C::kStages) * C::kStageBytes +
-                                                  C::kPoolBytes);
+                                                  2 * size_t(C::kPoolFloats) * 4);
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int h = tid % H;       // indexer head of this thread
     const int gl = tid / H;      // group within the tile
+    // Each CTA walks one contiguous range of tiles: it meets at most a couple
+    // of queries (few reloads of q) and streams its keys sequentially.
     const int total = a.batch * tiles_per_q;
-    const int step = gridDim.x;
+    const int t_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
+    const int t_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
 
     if (blockIdx.x == 0) {
         for (int b = tid; b < a.batch; b += blockDim.x) {
@@ -106,17 +132,23 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     __syncthreads();
 
     // Producer state lives in thread 0: the next tile to issue.
-    int t_issue = blockIdx.x;
+    int t_issue = t_begin;
     int n_issued = 0;
+    QueryCache qc_issue;
+    int64_t koff_b = -1, koff = 0;
     auto issue = [&](int stage) {
         TileRef r;
-        t_issue = next_tile<C::kTG>(a, t_issue, step, total, tiles_per_q, r);
-        if (t_issue >= total) return;
-        const float *src = a.idx_keys + (__ldg(a.key_offset + r.b) + int64_t(r.g0) * kGroup) * D;
+        t_issue = next_tile<C::kTG>(a, t_issue, t_end, tiles_per_q, qc_issue, r);
+        if (t_issue >= t_end) return;
+        if (r.b != koff_b) {
+            koff = __ldg(a.key_offset + r.b);
+            koff_b = r.b;
+        }
+        const float *src = a.idx_keys + (koff + int64_t(r.g0) * kGroup) * D;
         const uint32_t bytes = uint32_t(r.n) * C::kGroupFloats * 4u;
         mbar_arrive_expect_tx(&full[stage], bytes);
         bulk_copy_g2s(stages + size_t(stage) * C::kStageFloats, src, bytes, &full[stage]);
-        t_issue += step;
+        ++t_issue;
         ++n_issued;
     };
     if (tid == 0)
@@ -124,21 +156,23 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
     float qreg[D];
     int cur_b = -1;
-    int t_cons = blockIdx.x;
+    QueryCache qc;
+    int t_cons = t_begin;
     int it = 0;
     bool timed_out = false;
 
     while (true) {
         TileRef r;
-        t_cons = next_tile<C::kTG>(a, t_cons, step, total, tiles_per_q, r);
-        if (t_cons >= total) break;
+        t_cons = next_tile<C::kTG>(a, t_cons, t_end, tiles_per_q, qc, r);
+        if (t_cons >= t_end) break;
         const int s = it % C::kStages;
         const uint32_t parity = uint32_t(it / C::kStages) & 1u;
+        float *pool = pooled + (it & 1) * C::kPoolFloats;
 
         if (r.b != cur_b) {
             const float4 *qp = reinterpret_cast<const float4 *>(a.q_idx + (int64_t(r.b) * H + h) * D);
 #pragma unroll
-            for (int j4 = 0; j4 < D / 4; ++j4) {
+            for (int j4 = 0; j4 < F4; ++j4) {
                 const float4 v = __ldg(qp + j4);
                 qreg[4 * j4 + 0] = v.x;
                 qreg[4 * j4 + 1] = v.y;
@@ -150,32 +184,35 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
 
-        // Pool: element e of the tile's pooled block is (group e / D, lane e % D).
-        const float *raw = stages + size_t(s) * C::kStageFloats;
-        for (int e = tid; e < r.n * D; e += C::kThreads) {
-            const int g = e / D;
-            const int j = e - g * D;
-            const float *k = raw + g * C::kGroupFloats + j;
-            float acc = k[0];
-            acc = __fadd_rn(acc, k[D]);
-            acc = __fadd_rn(acc, k[2 * D]);
-            acc = __fadd_rn(acc, k[3 * D]);
-            pooled[g * C::kPoolStride + j] = __fmul_rn(acc, 0.25f);
+        // Pool, 16 bytes per item: item e is (group e / F4, chunk e % F4).
+        const float4 *raw = reinterpret_cast<const float4 *>(stages + size_t(s) * C::kStageFloats);
+        for (int e = tid; e < r.n * F4; e += C::kThreads) {
+            const int g = e / F4;
+            const int j4 = e - g * F4;
+            const float4 *k = raw + g * (kGroup * F4) + j4;
+            const float4 k0 = k[0], k1 = k[F4], k2 = k[2 * F4], k3 = k[3 * F4];
+            float4 p;
+            p.x = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.x, k1.x), k2.x), k3.x), 0.25f);
+            p.y = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.y, k1.y), k2.y), k3.y), 0.25f);
+            p.z = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.z, k1.z), k2.z), k3.z), 0.25f);
+            p.w = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.w, k1.w), k2.w), k3.w), 0.25f);
+            *reinterpret_cast<float4 *>(pool + pool_index<D>(g, j4)) = p;
         }
+        // One barrier per tile: the pooled tile is ready and raw stage s is
+        // consumed.  (The pooled tile is double buffered, so the next tile's
+        // pooling cannot overwrite what slower threads still read.)
         if (__syncthreads_or(!ok)) {
             timed_out = true;
             break;
         }
-        // Stage s is free again: refill it with the tile kStages ahead.
-        if (tid == 0) issue(s);
+        if (tid == 0) issue(s);  // refill stage s with the tile kStages ahead
 
         float relu = 0.0f;
         if (gl < r.n) {
-            const float *pg = pooled + gl * C::kPoolStride;
             float acc = 0.0f;
 #pragma unroll
-            for (int j4 = 0; j4 < D / 4; ++j4) {
-                const float4 pv = *reinterpret_cast<const float4 *>(pg + 4 * j4);
+            for (int j4 = 0; j4 < F4; ++j4) {
+                const float4 pv = *reinterpret_cast<const float4 *>(pool + pool_index<D>(gl, j4));
                 acc = __fmaf_rn(qreg[4 * j4 + 0], pv.x, acc);
                 acc = __fmaf_rn(qreg[4 * j4 + 1], pv.y, acc);
                 acc = __fmaf_rn(qreg[4 * j4 + 2], pv.z, acc);
@@ -185,13 +222,15 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         }
         // Head sum, h = 0..H-1 in order, gathered from the H lanes of the group.
         const int base = lane & ~(H - 1);
+        float hv[H];
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh) hv[hh] = __shfl_sync(0xffffffffu, relu, base + hh);
         float sum = 0.0f;
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, relu, base + hh));
+        for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, hv[hh]);
         if (h == 0 && gl < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + gl] = sum;
 
-        __syncthreads();  // pooled block is rewritten by the next tile
-        t_cons += step;
+        ++t_cons;
         ++it;
     }
 
@@ -212,16 +251,21 @@ cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
     const long long total = (long long)a.batch * tiles_per_q;
     if (total == 0) return cudaSuccess;
     if (total > 0x7fffffffLL) return cudaErrorInvalidValue;
-    static bool attr_done[64] = {};
+    static int resident[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (resident[dev] == 0) {
         cudaError_t e = cudaFuncSetAttribute(score_groups_kernel<H, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
         if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_groups_kernel<H, D>, C::kThreads, C::kSmem);
+        if (e != cudaSuccess) return e;
+        resident[dev] = per_sm > 0 ? per_sm : 1;
     }
-    const int grid = int(total < num_sms ? total : num_sms);
+    const long long slots = (long long)num_sms * resident[dev];
+    const int grid = int(total < slots ? total : slots);
     score_groups_kernel<H, D><<<grid, C::kThreads, C::kSmem, s>>>(a, tiles_per_q);
     return cudaGetLastError();
 }

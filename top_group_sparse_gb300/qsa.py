@@ -17,7 +17,8 @@ __all__ = [
     "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
     "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
-    "qsa_select", "qsa_gather", "qsa_attend", "qsa_decode", "qsa_attend_noalloc", "make_dims",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode", "qsa_attend_noalloc",
+    "make_dims",
     "DeviceBatch",
     "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
     "QSA_DEVERR_WAIT_TIMEOUT",
@@ -106,6 +107,8 @@ def load(path: str | None = None):
     L.qsa_gather.restype = ctypes.c_int
     L.qsa_attend.argtypes = [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_attend.restype = ctypes.c_int
+    L.qsa_gather_attend.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_gather_attend.restype = ctypes.c_int
     L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode.restype = ctypes.c_int
     L.qsa_attend_noalloc.argtypes = [_DP, _P, _P, _P, _P, _P, _P]
@@ -232,6 +235,13 @@ def qsa_attend(dims, q, k_scr, v_scr, n_ids, out, ws, stream=None) -> int:
         _stream(stream)))
 
 
+def qsa_gather_attend(dims, inputs, ids, n_ids, k_scr, v_scr, out, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_gather_attend", load().qsa_gather_attend(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(k_scr), _ptr(v_scr),
+        _ptr(out), p, n, _stream(stream)))
+
+
 def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
     p, n = _ws(ws)
     return _check("qsa_decode", load().qsa_decode(
@@ -309,6 +319,10 @@ class DeviceBatch:
     def attend(self, stream=None):
         return qsa_attend(self.dims, self.q, self.k_scr, self.v_scr, self.n_ids, self.out,
                           self.ws, stream)
+
+    def gather_attend(self, stream=None):
+        return qsa_gather_attend(self.dims, self.inputs, self.ids, self.n_ids, self.k_scr,
+                                 self.v_scr, self.out, self.ws, stream)
 
     def decode(self, stream=None):
         return qsa_decode(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws, stream)
