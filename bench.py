@@ -7,9 +7,10 @@ groups, indexer 8 heads x 64, GQA attention 16 query / 2 KV heads x 128, all
 values N(0,1), K/V in a wrapped ring buffer (slot = (t + 131,072) mod
 262,144).  One step = one pass of the whole hot path over the batch: group
 scoring, set choice + chronological emission, slot resolution + compact
-gather, online-softmax attention -- the three C-ABI stage calls that
-qsa_decode issues (scoring, selection, fused gather + attention), with a
-CUDA event between stages.
+gather, online-softmax attention -- one qsa_decode call (three launches:
+scoring, selection, fused gather + attention), bracketed by CUDA events.
+Per-kernel durations come from a second pass through qsa_decode_profiled,
+which records an event before each of the three launches and after the last.
 
 Timing: W untimed warm-up steps, then K timed steps.  Before each timed step
 L2 is flushed (a 256 MiB buffer written, then another 256 MiB read), outside
@@ -243,14 +244,12 @@ def run_gpu(args):
         torch.sum(flush_r, dim=0, out=sink[0])
 
     def step(ev=None):
-        # exactly the launches of qsa_decode, one C-ABI stage call each
-        if ev is None:
-            db.score(stream); db.select(stream); db.gather_attend(stream)
-            return
-        ev[0].record(stream); db.score(stream)
-        ev[1].record(stream); db.select(stream)
-        ev[2].record(stream); db.gather_attend(stream)
-        ev[3].record(stream)
+        # one qsa_decode call; ev (two events) brackets it
+        if ev is not None:
+            ev[0].record(stream)
+        db.decode(stream)
+        if ev is not None:
+            ev[1].record(stream)
 
     for _ in range(args.warmup):
         flush()
@@ -258,7 +257,11 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for ev in events:  # create the CUDA events before the timed region
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier()
@@ -274,9 +277,24 @@ def run_gpu(args):
     if st != 0:
         raise SystemExit(f"device error word {flags:#x} after the timed loop")
 
-    step_ms = np.array([e[0].elapsed_time(e[3]) for e in events])
-    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in events])
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in events])
     total_ms = max_over_ranks(float(step_ms.sum()), db.out.device)
+
+    # ---- per-kernel durations: the same steps through qsa_decode_profiled -------
+    # (events between its three launches; this form gives up the overlap of
+    # launch latencies, so its sum is a little above the plain step)
+    K3 = max(1, min(K, 500))
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K3)]
+    for ev in pev:
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)
+    for k3 in range(K3):
+        flush()
+        db.decode_profiled(pev[k3], stream)
+    torch.cuda.synchronize()
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in pev])
     ms_per_step = total_ms / K
     value = ws * w.batch * K / (total_ms / 1e3)
 

@@ -120,8 +120,11 @@ typedef struct {
 /* Bytes of workspace every call below needs for these dims (0 if the dims
  * are invalid).  Sized as groups + budget + selected width per query,
  * never queries x keys ([AFN-016] What the checkpoint measures):
- *   header + B*score_stride*4 (scores) + 2*B*row_capacity*n_kv*d*4 (K/V
- *   scratch) + B*n_q*ceil(row_capacity/64)*(d+2)*4 (attention partials). */
+ *   header + B*score_stride*4 (scores) + B*qstride*4 (the largest score of
+ *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
+ *   to 32, G_max = max_visible/4) +
+ *   2*B*row_capacity*n_kv*d*4 (K/V scratch) +
+ *   B*n_q*8*(d+2)*4 (attention partials, 8 per head). */
 size_t qsa_workspace_size(const qsa_dims *dims);
 
 /* Row stride, in floats, of a scores buffer: max_visible/4 rounded up to 32. */
@@ -192,11 +195,11 @@ qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t 
  * makes order observable; [AFN-016] Decision).  For each query b and head h
  * (KV head h / (n_q/n_kv)):
  *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
- * rows i < n_ids[b] visited in emitted order: the row is cut into fixed
- * 64-row chunks, each reduced with a running max / rescale / denominator /
- * accumulator, and the chunk partials merged in ascending chunk order.  The
- * split depends only on n_ids[b], so results do not depend on the batch.
- * n_ids[b] = 0 gives a zero output.  out: [B, n_q, d]. */
+ * rows i < n_ids[b] visited in emitted order: the row is cut into 64-row
+ * sub-chunks grouped into 8 consecutive runs; each run is reduced with a
+ * running max / rescale / denominator / accumulator, and the 8 partials are
+ * merged in order.  The split depends only on n_ids[b], so results do not
+ * depend on the batch.  n_ids[b] = 0 gives a zero output.  out: [B, n_q, d]. */
 qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr,
                       const float *v_scr, const int32_t *n_ids, float *out,
                       void *ws, size_t ws_bytes, void *stream);
@@ -217,6 +220,15 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 
+/* qsa_decode with timing marks: `events` holds n_events = 4 cudaEvent_t
+ * handles (created by the caller) recorded on `stream` before the scoring
+ * launch, before the selection launch, before the gather + attention launch
+ * and after it; n_events = 0 is plain qsa_decode.  The launches and results
+ * are those of qsa_decode. */
+qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
+                               int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream,
+                               void *const *events, int32_t n_events);
+
 /* ---- attention without a workspace -------------------------------------- */
 
 /* Fixed size of the device scratch behind qsa_attend_noalloc (4 MiB); every
@@ -230,10 +242,10 @@ qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
  * runs.  Same arguments, kernel and results as qsa_attend, minus `ws`: the
  * error word, merge tickets and chunk partials live in one static device
  * array of QSA_ATTEND_NOALLOC_SCRATCH_BYTES.  Nothing is allocated or freed.
- *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*C*4)
- *    + align256(B*n_q*C*d*4) bytes must fit, C = ceil((4*budget+3)/64);
- *    larger dims return QSA_ERR_WORKSPACE_TOO_SMALL before anything is
- *    enqueued (e.g. B=8, n_q=16, d=128, budget 512 needs 2.2 MB: fits).
+ *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*8*4)
+ *    + align256(B*n_q*8*d*4) bytes must fit; larger dims return
+ *    QSA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (e.g. B=8,
+ *    n_q=16, d=128 needs 0.6 MB: fits; B=64 at the same shape does not).
  *  - The first call on each device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and keeps it; make that
  *    first call before any stream capture.

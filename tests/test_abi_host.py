@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 14
+    assert len(names) == 15
     for n in names:
         assert hasattr(lib, n), n
     for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",
@@ -59,14 +59,14 @@ def test_workspace_formula(lib):
     keys ("A sparse mask is not sparse attention", What the checkpoint measures)."""
     d = _dims()
     B, nq, nkv, hd, cap = 8, 16, 2, 128, 2051
-    nch = -(-cap // 64)
+    nch = 8  # attention partials per head
     want = 256 + _align(B * nkv * 4) + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
-        + _align(B * 65536 * 4) + 2 * _align(B * cap * nkv * hd * 4)
+        + _align(B * 16384 * 4) + _align(B * 65536 * 4) + 2 * _align(B * cap * nkv * hd * 4)
     assert qsa.qsa_workspace_size(d) == want
-    # doubling the history adds exactly the scores of the new groups
+    # doubling the history adds exactly the scores (and per-quad maxima) of the new groups
     a = qsa.qsa_workspace_size(_dims(max_visible=1 << 20))
     b = qsa.qsa_workspace_size(_dims(max_visible=1 << 21))
-    assert b - a == B * ((1 << 19) - (1 << 18)) * 4
+    assert b - a == B * ((1 << 19) - (1 << 18)) * 4 + B * ((1 << 17) - (1 << 16)) * 4
     # and is linear in the batch
     assert qsa.qsa_workspace_size(_dims(batch=16)) < 2 * qsa.qsa_workspace_size(d) + 4096
 

@@ -208,3 +208,29 @@ def test_gather_attend_equals_gather_then_attend(shape):
     gpu = {"ids": db.ids.cpu().numpy(), "n_ids": n, "out": db.out.cpu().numpy()}
     assert_ids_equal(w, gpu, ref)
     assert_attention_close(w, gpu, ref)
+
+
+def test_decode_profiled_matches_decode():
+    """The instrumented decode issues the same launches: same bits, and its four
+    events bracket the three stages in order."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    w = wl.make_workload("prof", [30001, 65537, 2052, 5], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=61, slots="ring", ring_size=70000,
+                         ring_shift=999)
+    db = qsa.DeviceBatch(w)
+    db.decode()
+    torch.cuda.synchronize()
+    ids, out = db.ids.clone(), db.out.clone()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    db.out.fill_(float("nan"))
+    db.decode_profiled(ev)
+    torch.cuda.synchronize()
+    assert torch.equal(db.ids, ids) and torch.equal(db.out, out)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(t > 0 for t in times)
+    assert db.check_errors() == (0, 0)
+    ref = oracle_run(w)
+    gpu = {"ids": db.ids.cpu().numpy(), "n_ids": db.n_ids.cpu().numpy(), "out": db.out.cpu().numpy()}
+    assert_ids_equal(w, gpu, ref)
+    assert_attention_close(w, gpu, ref)

@@ -33,20 +33,24 @@ Layout make_layout(const qsa_dims *d)
     L.score_stride = ((gmax + 31) / 32) * 32;
     if (L.score_stride == 0) L.score_stride = 32;
     L.row_cap = kGroup * d->budget_groups + (kGroup - 1);
-    L.nchunk_max = (L.row_cap + kAttendChunk - 1) / kAttendChunk;
+    L.nparts = kAttendParts;
     const size_t B = size_t(d->batch);
     size_t off = 0;
     L.off_err = off;
     off += kWsAlign;
     L.off_tickets = off;
     off = align_up(off + B * size_t(d->kv_heads) * 4, kWsAlign);
-    const size_t nparts = B * size_t(d->q_heads) * size_t(L.nchunk_max);
+    const size_t nparts = B * size_t(d->q_heads) * size_t(L.nparts);
     L.off_part_m = off;
     off = align_up(off + nparts * 4, kWsAlign);
     L.off_part_l = off;
     off = align_up(off + nparts * 4, kWsAlign);
     L.off_part_acc = off;
     off = align_up(off + nparts * size_t(d->head_dim) * 4, kWsAlign);
+    L.qmax_stride = ((gmax + 3) / 4 + 31) / 32 * 32;
+    if (L.qmax_stride == 0) L.qmax_stride = 32;
+    L.off_qmax = off;
+    off = align_up(off + B * size_t(L.qmax_stride) * 4, kWsAlign);
     L.off_scores = off;
     off = align_up(off + B * size_t(L.score_stride) * 4, kWsAlign);
     const size_t scr = B * size_t(L.row_cap) * size_t(d->kv_heads) * size_t(d->head_dim) * 4;
@@ -123,17 +127,22 @@ qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int6
     const int sms = num_sms_of_current_device();
     if (sms <= 0) return QSA_ERR_CUDA;
     ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, stride,
-                d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L)};
+                d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L),
+                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride};
     return from_cuda(launch_score(a, sms, s));
 }
 
+// use_hint: the quad maxima in the workspace were written by the scorer for
+// exactly these scores (only inside qsa_decode).
 qsa_status do_select(const qsa_dims *d, const int32_t *visible, const float *scores, int64_t stride,
-                     int32_t *ids, int32_t *n_ids, void *ws, const Layout &L, cudaStream_t s)
+                     int32_t *ids, int32_t *n_ids, void *ws, const Layout &L, cudaStream_t s, bool use_hint,
+                     bool pdl = false)
 {
     if (d->batch == 0) return QSA_OK;
     SelectArgs a{visible, scores, stride, ids, n_ids, L.row_cap, d->budget_groups, d->max_visible,
-                 d->batch, err_word(ws, L)};
-    return from_cuda(launch_select(a, s));
+                 d->batch, err_word(ws, L), use_hint ? ws_at<uint32_t>(ws, L.off_qmax) : nullptr,
+                 L.qmax_stride};
+    return from_cuda(launch_select(a, s, pdl));
 }
 
 qsa_status do_gather(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
@@ -153,23 +162,24 @@ qsa_status do_attend(const qsa_dims *d, const float *q, const float *k_scr, cons
     AttendArgs a{q, k_scr, v_scr, n_ids, out,
                  ws_at<float>(ws, L.off_part_m), ws_at<float>(ws, L.off_part_l),
                  ws_at<float>(ws, L.off_part_acc), ws_at<uint32_t>(ws, L.off_tickets),
-                 L.row_cap, L.nchunk_max, d->batch, d->q_heads, d->kv_heads, d->head_dim,
+                 L.row_cap, L.nparts, d->batch, d->q_heads, d->kv_heads, d->head_dim,
                  d->scale, err_word(ws, L)};
     return from_cuda(launch_attend(a, s));
 }
 
 qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
-                            float *k_scr, float *v_scr, float *out, void *ws, const Layout &L, cudaStream_t s)
+                            float *k_scr, float *v_scr, float *out, void *ws, const Layout &L, cudaStream_t s,
+                            bool pdl = false)
 {
     if (d->batch == 0) return QSA_OK;
     AttendArgs a{in->q, nullptr, nullptr, n_ids, out,
                  ws_at<float>(ws, L.off_part_m), ws_at<float>(ws, L.off_part_l),
                  ws_at<float>(ws, L.off_part_acc), ws_at<uint32_t>(ws, L.off_tickets),
-                 L.row_cap, L.nchunk_max, d->batch, d->q_heads, d->kv_heads, d->head_dim,
+                 L.row_cap, L.nparts, d->batch, d->q_heads, d->kv_heads, d->head_dim,
                  d->scale, err_word(ws, L),
                  ids, in->visible, in->slot_map, in->slot_offset, in->k_cache, in->v_cache, in->num_slots,
                  k_scr, v_scr};
-    return from_cuda(launch_attend(a, s));
+    return from_cuda(launch_attend(a, s, pdl));
 }
 
 qsa_status check_shapes(const qsa_dims *d, bool score, bool attend)
@@ -286,7 +296,7 @@ qsa_status qsa_select(const qsa_dims *dims, const int32_t *visible, const float 
     if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
     const Layout L = make_layout(dims);
     return do_select(dims, visible, scores, L.score_stride, ids, n_ids, ws, L,
-                     static_cast<cudaStream_t>(stream));
+                     static_cast<cudaStream_t>(stream), false);
 }
 
 qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
@@ -335,8 +345,9 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
     return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, static_cast<cudaStream_t>(stream));
 }
 
-qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids, float *out,
-                      void *ws, size_t ws_bytes, void *stream)
+qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids,
+                               float *out, void *ws, size_t ws_bytes, void *stream, void *const *events,
+                               int32_t n_events)
 {
     if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
     qsa_status st;
@@ -347,14 +358,35 @@ qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, 
     if (!ids || !n_ids || !out || !aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(out, 16))
         return QSA_ERR_INVALID_ARG;
     if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    if (n_events != 0 && (n_events != 4 || !events)) return QSA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_events; ++i)
+        if (!events[i]) return QSA_ERR_INVALID_ARG;
     const Layout L = make_layout(dims);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *scores = ws_at<float>(ws, L.off_scores);
     float *k_scr = ws_at<float>(ws, L.off_kscr);
     float *v_scr = ws_at<float>(ws, L.off_vscr);
+    auto mark = [&](int i) -> bool {
+        return n_events == 0 || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
+    if (!mark(0)) return QSA_ERR_CUDA;
     if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s)) != QSA_OK) return st;
-    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s)) != QSA_OK) return st;
-    return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, s);
+    if (!mark(1)) return QSA_ERR_CUDA;
+    // The three launches overlap their launch latency with the predecessor's
+    // tail (programmatic dependent launch) unless timing marks separate them.
+    const bool pdl = n_events == 0;
+    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s, true, pdl)) != QSA_OK)
+        return st;
+    if (!mark(2)) return QSA_ERR_CUDA;
+    if ((st = do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, s, pdl)) != QSA_OK) return st;
+    if (!mark(3)) return QSA_ERR_CUDA;
+    return QSA_OK;
+}
+
+qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids, float *out,
+                      void *ws, size_t ws_bytes, void *stream)
+{
+    return qsa_decode_profiled(dims, in, ids, n_ids, out, ws, ws_bytes, stream, nullptr, 0);
 }
 
 }  // extern "C"

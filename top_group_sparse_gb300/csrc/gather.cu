@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(kThreads)
 gather_kernel(const GatherArgs a)
 {
     const int b = blockIdx.y;
-    const int n = __ldg(a.n_ids + b);
+    const int n = __ldcg(a.n_ids + b);
     const int T = __ldg(a.visible + b);
     if (n < 0 || n > a.row_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, QSA_DEVERR_ROW_RANGE);
@@ -52,7 +52,7 @@ gather_kernel(const GatherArgs a)
         if (e >= limit) continue;
         const int i = int(e / f4);
         const int p = int(e - int64_t(i) * f4);
-        const int id = __ldg(ids + i);
+        const int id = __ldcg(ids + i);
         const bool id_ok = id >= 0 && id < T;
         const int64_t slot = id_ok ? int64_t(__ldg(smap + id)) : -1;
         dst[u] = e;

@@ -33,11 +33,11 @@ struct StaticLayout {
     size_t off_err, off_tickets, off_part_m, off_part_l, off_part_acc, header_bytes, total;
 };
 
-StaticLayout static_layout(const qsa_dims *d, int32_t nchunk_max)
+StaticLayout static_layout(const qsa_dims *d, int32_t nparts_per_head)
 {
     StaticLayout L{};
     const size_t B = size_t(d->batch);
-    const size_t nparts = B * size_t(d->q_heads) * size_t(nchunk_max);
+    const size_t nparts = B * size_t(d->q_heads) * size_t(nparts_per_head);
     size_t off = 0;
     L.off_err = off;
     off += kWsAlign;
@@ -95,7 +95,7 @@ extern "C" qsa_status qsa_attend_noalloc(const qsa_dims *dims, const float *q, c
         (reinterpret_cast<uintptr_t>(out) & 15u) != 0)
         return QSA_ERR_INVALID_ARG;
     const Layout W = make_layout(dims);  // row capacity and chunk count, as qsa_attend
-    const StaticLayout L = static_layout(dims, W.nchunk_max);
+    const StaticLayout L = static_layout(dims, W.nparts);
     if (L.total > kStaticScratchBytes) return QSA_ERR_WORKSPACE_TOO_SMALL;  // beyond the fixed maximum
     if (dims->batch == 0) return QSA_OK;
 
@@ -108,7 +108,7 @@ extern "C" qsa_status qsa_attend_noalloc(const qsa_dims *dims, const float *q, c
     AttendArgs a{q, k_scr, v_scr, n_ids, out,
                  reinterpret_cast<float *>(s + L.off_part_m), reinterpret_cast<float *>(s + L.off_part_l),
                  reinterpret_cast<float *>(s + L.off_part_acc), reinterpret_cast<uint32_t *>(s + L.off_tickets),
-                 W.row_cap, W.nchunk_max, dims->batch, dims->q_heads, dims->kv_heads, dims->head_dim,
+                 W.row_cap, W.nparts, dims->batch, dims->q_heads, dims->kv_heads, dims->head_dim,
                  dims->scale, reinterpret_cast<uint32_t *>(s + L.off_err)};
     return launch_attend(a, st) == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "qsa.h"
 
 namespace qsa {
@@ -15,19 +17,40 @@ namespace qsa {
 // ---- workspace layout -----------------------------------------------------
 
 constexpr int kGroup = 4;            // tokens per scored group
-constexpr int kAttendChunk = 64;     // rows per attention chunk (fixed: the split
-                                     // depends on the row length only)
+constexpr int kAttendChunk = 64;     // rows per attention sub-chunk
+constexpr int kAttendParts = 8;      // attention CTAs (and partials) per (query, KV head);
+                                     // the split depends on the row length only
 constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
 constexpr size_t kWsAlign = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launches kernel<<<grid, block, smem, s>>>(args...), optionally with the
+// programmatic stream-serialization attribute (see wait_for_predecessor).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool pdl, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 struct Layout {
     int64_t score_stride;   // floats per scores row
+    int64_t qmax_stride;    // entries per row of quad maxima (selection hint)
     int32_t row_cap;        // IDs per row: 4*budget + 3
-    int32_t nchunk_max;     // attention chunks per row at full capacity
+    int32_t nparts;         // attention partials per (query, head): kAttendParts
     size_t off_err, off_tickets, off_part_m, off_part_l, off_part_acc;
-    size_t off_scores, off_kscr, off_vscr;
+    size_t off_qmax, off_scores, off_kscr, off_vscr;
     size_t total;
 };
 
@@ -45,9 +68,14 @@ struct ScoreArgs {
     int64_t score_stride;
     int32_t batch, idx_heads, idx_dim, max_visible;
     uint32_t *err;
+    uint32_t *qmax;          // [B, qmax_stride]: order key of the max score of groups 4j..4j+3
+    int64_t qmax_stride;
 };
 bool score_shape_supported(int idx_heads, int idx_dim);
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
+
+// pdl: launch programmatically after the previous kernel in the stream
+// (used only inside qsa_decode, where the order of the launches is fixed).
 
 struct SelectArgs {
     const int32_t *visible;
@@ -57,8 +85,10 @@ struct SelectArgs {
     int32_t *n_ids;
     int32_t row_cap, budget, max_visible, batch;
     uint32_t *err;
+    const uint32_t *qmax;    // hint only: quad maxima as written by the scorer (may be stale)
+    int64_t qmax_stride;
 };
-cudaError_t launch_select(const SelectArgs &a, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs &a, cudaStream_t s, bool pdl = false);
 
 struct GatherArgs {
     const int32_t *visible;
@@ -81,7 +111,7 @@ struct AttendArgs {
     float *out;
     float *part_m, *part_l, *part_acc;
     uint32_t *tickets;
-    int32_t row_cap, nchunk_max, batch, q_heads, kv_heads, head_dim;
+    int32_t row_cap, nparts, batch, q_heads, kv_heads, head_dim;
     float scale;
     uint32_t *err;
     // fused gather: when k_cache != nullptr, rows are resolved through the slot
@@ -95,9 +125,17 @@ struct AttendArgs {
     float *k_scr_out, *v_scr_out;
 };
 bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
-cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s);
+cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl = false);
 
 // ---- device helpers ---------------------------------------------------------
+
+// Order-preserving uint32 image of a score: larger float, larger key; -0 is
+// folded to +0 first.  Scores from the scorer are in [+0, +inf].
+__device__ __forceinline__ uint32_t order_key(float x)
+{
+    const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bit)
 {
@@ -170,6 +208,22 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor drains; it
+// must wait here before touching anything the predecessor writes.  Both
+// instructions are no-ops for a kernel launched the ordinary way.
+__device__ __forceinline__ void wait_for_predecessor()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream (if launched programmatically) begin
+// launching; its CTAs still wait in wait_for_predecessor() for this grid.
+__device__ __forceinline__ void allow_successor_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;     // 1 s for a copy to land

@@ -43,7 +43,8 @@ struct ScoreCfg {
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kPoolFloats = kTG * D;             // one pooled tile (swizzled)
     static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * size_t(kPoolFloats) * 4 + kStages * 8;
-    static_assert(kThreads % H == 0 && 32 % H == 0, "heads must divide a warp");
+    static_assert(kThreads % H == 0 && 32 % (4 * H) == 0, "a warp holds whole quads of groups");
+    static_assert(kTG % 4 == 0, "tiles start on quad boundaries");
     static_assert(D % 32 == 0, "the pooled-tile swizzle needs D/4 to be a multiple of 8");
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
@@ -119,6 +120,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     const int t_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
     const int t_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
 
+    allow_successor_launch();  // selection CTAs fill SMs as this grid's CTAs retire
     if (blockIdx.x == 0) {
         for (int b = tid; b < a.batch; b += blockDim.x) {
             const int T = __ldg(a.visible + b);
@@ -229,6 +231,13 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, hv[hh]);
         if (h == 0 && gl < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + gl] = sum;
+        // Selection hint: the largest key among groups 4j..4j+3 (the H-lane
+        // blocks of those four groups sit side by side in the warp).
+        uint32_t qk = (gl < r.n) ? order_key(sum) : 0u;
+        qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, H));
+        qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, 2 * H));
+        if ((lane & (4 * H - 1)) == 0 && gl < r.n)
+            a.qmax[int64_t(r.b) * a.qmax_stride + ((r.g0 + gl) >> 2)] = qk;
 
         ++t_cons;
         ++it;

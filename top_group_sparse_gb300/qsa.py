@@ -17,7 +17,8 @@ __all__ = [
     "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
     "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
-    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode", "qsa_attend_noalloc",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode",
+    "qsa_decode_profiled", "qsa_attend_noalloc",
     "make_dims",
     "DeviceBatch",
     "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
@@ -111,6 +112,9 @@ def load(path: str | None = None):
     L.qsa_gather_attend.restype = ctypes.c_int
     L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode.restype = ctypes.c_int
+    L.qsa_decode_profiled.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                      ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32]
+    L.qsa_decode_profiled.restype = ctypes.c_int
     L.qsa_attend_noalloc.argtypes = [_DP, _P, _P, _P, _P, _P, _P]
     L.qsa_attend_noalloc.restype = ctypes.c_int
     if path is None:
@@ -249,6 +253,23 @@ def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
         _stream(stream)))
 
 
+def qsa_decode_profiled(dims, inputs, ids, n_ids, out, ws, events, stream=None) -> int:
+    """events: four torch.cuda.Event(enable_timing=True) (or raw cudaEvent_t ints)."""
+    handles = []
+    for e in events:
+        if isinstance(e, int):
+            handles.append(e)
+        else:
+            if not e.cuda_event:  # torch creates the CUDA event on first record
+                e.record()
+            handles.append(int(e.cuda_event))
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    p, n = _ws(ws)
+    return _check("qsa_decode_profiled", load().qsa_decode_profiled(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(out), p, n,
+        _stream(stream), arr, len(handles)))
+
+
 def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
     """Attention stage with the library's fixed static scratch instead of a
     workspace, for callers that cannot allocate device memory."""
@@ -326,6 +347,10 @@ class DeviceBatch:
 
     def decode(self, stream=None):
         return qsa_decode(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws, stream)
+
+    def decode_profiled(self, events, stream=None):
+        return qsa_decode_profiled(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws,
+                                   events, stream)
 
     def check_errors(self, stream=None):
         return qsa_check_errors(self.ws, stream)
