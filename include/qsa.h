@@ -123,8 +123,9 @@ typedef struct {
  *   header + B*score_stride*4 (scores) + B*qstride*4 (the largest score of
  *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
  *   to 32, G_max = max_visible/4) +
- *   2*B*row_capacity*n_kv*d*4 (K/V scratch) +
- *   B*n_q*8*(d+2)*4 (attention partials, 8 per head). */
+ *   B*n_q*9*(d+2)*4 (attention partials: 9 runs of 256 rows per head).
+ * The compact K/V row of qsa_decode never reaches device memory, so the
+ * workspace holds no K/V scratch. */
 size_t qsa_workspace_size(const qsa_dims *dims);
 
 /* Row stride, in floats, of a scores buffer: max_visible/4 rounded up to 32. */
@@ -195,28 +196,34 @@ qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t 
  * makes order observable; [AFN-016] Decision).  For each query b and head h
  * (KV head h / (n_q/n_kv)):
  *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
- * rows i < n_ids[b] visited in emitted order: the row is cut into 64-row
- * sub-chunks grouped into 8 consecutive runs; each run is reduced with a
- * running max / rescale / denominator / accumulator, and the 8 partials are
- * merged in order.  The split depends only on n_ids[b], so results do not
- * depend on the batch.  n_ids[b] = 0 gives a zero output.  out: [B, n_q, d]. */
+ * rows i < n_ids[b] visited in emitted order: the row is cut into runs of
+ * 256 rows (9 at most), each run into groups of 32/r consecutive rows
+ * (r = n_q/n_kv) dealt to 8 running states in turn; each state is a running
+ * max / rescale / denominator / accumulator, and the states are merged in a
+ * fixed order, then the runs in row order.  The split depends only on
+ * n_ids[b], so results do not depend on the batch.  n_ids[b] = 0 gives a
+ * zero output.  out: [B, n_q, d]. */
 qsa_status qsa_attend(const qsa_dims *dims, const float *q, const float *k_scr,
                       const float *v_scr, const int32_t *n_ids, float *out,
                       void *ws, size_t ws_bytes, void *stream);
 
 /* Stages 3 and 4 in one launch: each attention CTA resolves its rows'
- * slots, copies exactly those K/V rows from the cache, writes them to
- * k_scr / v_scr (the same bytes as qsa_gather) and runs the attention of
- * qsa_attend on them from on-chip memory.  Outputs: k_scr, v_scr (as
+ * slots, copies exactly those K/V rows from the cache into shared memory,
+ * writes them from there to k_scr / v_scr (the same bytes as qsa_gather) and
+ * runs the attention of qsa_attend on them.  Outputs: k_scr, v_scr (as
  * qsa_gather) and out (as qsa_attend), bit-identical to qsa_gather followed
  * by qsa_attend. */
 qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids,
                              const int32_t *n_ids, float *k_scr, float *v_scr, float *out,
                              void *ws, size_t ws_bytes, void *stream);
 
-/* The whole path on `stream`: qsa_score_groups, qsa_select and
- * qsa_gather_attend back to back, with scores and K/V scratch kept in the
- * workspace.  Outputs: ids, n_ids (as qsa_select) and out (as qsa_attend). */
+/* The whole path on `stream`: qsa_score_groups, qsa_select, then the
+ * gather fused into the attention ([AFN-016] Why compact gather comes before
+ * fusion: fusion once the compact path is measured, keeping logical IDs and
+ * zero dense-mask bytes) -- each attention CTA copies its selected K/V rows
+ * from the cache straight into shared memory, so the compact row is never
+ * written to device memory.  Outputs: ids, n_ids (as qsa_select) and out,
+ * bit-identical to qsa_attend over qsa_gather's scratch. */
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 
@@ -242,8 +249,8 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
  * runs.  Same arguments, kernel and results as qsa_attend, minus `ws`: the
  * error word, merge tickets and chunk partials live in one static device
  * array of QSA_ATTEND_NOALLOC_SCRATCH_BYTES.  Nothing is allocated or freed.
- *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*8*4)
- *    + align256(B*n_q*8*d*4) bytes must fit; larger dims return
+ *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*9*4)
+ *    + align256(B*n_q*9*d*4) bytes must fit; larger dims return
  *    QSA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (e.g. B=8,
  *    n_q=16, d=128 needs 0.6 MB: fits; B=64 at the same shape does not).
  *  - The first call on each device, with that device current, looks up the

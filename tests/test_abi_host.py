@@ -56,12 +56,13 @@ def _align(x, a=256):
 
 def test_workspace_formula(lib):
     """Scratch is groups + budget + selected width per query, never queries x
-    keys ("A sparse mask is not sparse attention", What the checkpoint measures)."""
+    keys ("A sparse mask is not sparse attention", What the checkpoint measures);
+    the compact K/V row of the whole-path call stays on chip, so no K/V scratch."""
     d = _dims()
-    B, nq, nkv, hd, cap = 8, 16, 2, 128, 2051
-    nch = 8  # attention partials per head
+    B, nq, nkv, hd = 8, 16, 2, 128
+    nch = 9  # attention partials per head: runs of 256 rows over at most 2051 rows
     want = 256 + _align(B * nkv * 4) + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
-        + _align(B * 16384 * 4) + _align(B * 65536 * 4) + 2 * _align(B * cap * nkv * hd * 4)
+        + _align(B * 16384 * 4) + _align(B * 65536 * 4)
     assert qsa.qsa_workspace_size(d) == want
     # doubling the history adds exactly the scores (and per-quad maxima) of the new groups
     a = qsa.qsa_workspace_size(_dims(max_visible=1 << 20))

@@ -53,11 +53,6 @@ Layout make_layout(const qsa_dims *d)
     off = align_up(off + B * size_t(L.qmax_stride) * 4, kWsAlign);
     L.off_scores = off;
     off = align_up(off + B * size_t(L.score_stride) * 4, kWsAlign);
-    const size_t scr = B * size_t(L.row_cap) * size_t(d->kv_heads) * size_t(d->head_dim) * 4;
-    L.off_kscr = off;
-    off = align_up(off + scr, kWsAlign);
-    L.off_vscr = off;
-    off = align_up(off + scr, kWsAlign);
     L.total = off;
     return L;
 }
@@ -364,8 +359,6 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
     const Layout L = make_layout(dims);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float *scores = ws_at<float>(ws, L.off_scores);
-    float *k_scr = ws_at<float>(ws, L.off_kscr);
-    float *v_scr = ws_at<float>(ws, L.off_vscr);
     auto mark = [&](int i) -> bool {
         return n_events == 0 || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     };
@@ -378,7 +371,8 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
     if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s, true, pdl)) != QSA_OK)
         return st;
     if (!mark(2)) return QSA_ERR_CUDA;
-    if ((st = do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, s, pdl)) != QSA_OK) return st;
+    // K/V rows go from the cache to shared memory and nowhere else: no scratch
+    if ((st = do_gather_attend(dims, in, ids, n_ids, nullptr, nullptr, out, ws, L, s, pdl)) != QSA_OK) return st;
     if (!mark(3)) return QSA_ERR_CUDA;
     return QSA_OK;
 }

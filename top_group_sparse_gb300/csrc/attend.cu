@@ -7,35 +7,42 @@
 // visit order is needed -- the emitted, chronological one.  "A sparse mask is
 // not sparse attention" (AFN-016), Decision: online softmax over at most
 // 2,051 gathered rows; only the gather crosses from logical identity into the
-// physical cache layout, and it copies exactly the selected rows into bounded
-// scratch (Why compact gather comes before fusion).
+// physical cache layout.
 //
 // GPU order (fixed, documented, batch independent).  The emitted row of
-// query b is cut into sub-chunks of 64 consecutive rows, and the sub-chunks
-// into kParts consecutive runs, one per CTA working on (query b, KV head); the
-// split depends only on n_ids[b].  Each CTA walks its sub-chunks in row order
-// with an online softmax for the n_q/n_kv query heads of that KV head: per
-// sub-chunk, scaled scores x_i, the new running max m' = max(m, max x_i), the
+// query b is cut into runs of kRowsPerPart consecutive rows, one CTA per
+// (run, query b, KV head); the cut depends only on n_ids[b].  A run is cut
+// into steps of 8 consecutive rows, and step j goes to warp j mod 8, which
+// keeps its own online-softmax state for the GQ query heads of the KV head:
+// per step, scaled scores x_i, the new running max m' = max(m, max x_i), the
 // rescale e^(m - m') of the denominator l and of the accumulator, then
-// l += sum_i e^(x_i - m') and acc += sum_i e^(x_i - m') v_i.  The last CTA of
-// the (query, KV head) to finish -- an atomic ticket, nothing waits -- merges
-// the kParts partials in order: M = max m_p, L = sum l_p e^(m_p - M),
-// out = sum acc_p e^(m_p - M) / L.  No floating-point atomics; the bits of a
-// query's output do not depend on the rest of the batch.
+// l += sum_i e^(x_i - m') and acc += sum_i e^(x_i - m') v_i.  At the end of
+// the run the eight warp states are merged in warp order (M = max m_w,
+// L = sum l_w e^(m_w - M), acc = sum acc_w e^(m_w - M)), and the last CTA of
+// the (query, KV head) to finish -- an atomic ticket, nothing waits --
+// merges the runs in order the same way and divides by L.  No floating-point
+// atomics; the bits of a query's output do not depend on the rest of the batch.
 //
-// Layout of a CTA: eight warps.  They resolve all of the CTA's rows once (every
-// ID load, then every slot load) and stream the K/V sub-chunks through a
-// two-stage ring in shared memory with 16-byte asynchronous copies (four
-// threads per row, so each row read is one contiguous 512-byte run).  In the
-// math a lane owns one 16-byte column of a row: the query heads' slices of
-// that column live in registers, a warp forms R rows x GQ heads = 32 partial
-// dot products at a time and a 31-shuffle reduce-scatter leaves each lane one
-// finished score; for P.V each warp takes 8 rows of the sub-chunk for every head.
-// Row source: kFromCache = false reads the gathered scratch (qsa_attend);
-// kFromCache = true resolves each ID through the slot map, copies the row
-// from the K/V cache, and the threads write their pieces of it to the scratch
-// from shared memory (qsa_gather_attend, qsa_decode) -- the gather's output is
-// the same bytes either way.
+// Data movement: the CTA's 256 threads resolve every row of its run at once
+// (one row each: the ID load, then the slot-map load).  Each warp then
+// streams only its own steps through its own three-slot ring in shared
+// memory with 16-byte asynchronous copies, two steps ahead of its math, so no
+// thread-block barrier and no cross-warp wait sits inside the loop.
+//
+// Math of a step (8 rows x GQ heads).  Scores: lanes form HP = min(GQ, 4)
+// head groups of DS = 32/HP lanes; a lane holds HPL = GQ/HP heads of the query
+// in registers, restricted to its d-slice (16-byte columns ds, ds + DS, ...),
+// forms 8 x HPL partial dot products, and a reduce-scatter over the DS lanes
+// of its group leaves it the finished dots of one row (ds, for GQ >= 4) and
+// its HPL heads.  Weighted values: a lane owns one 16-byte column of V for
+// all GQ heads.
+//
+// Row source: Src::kScratch reads the gathered scratch (qsa_attend);
+// Src::kCache resolves each ID through the slot map and copies the row from
+// the K/V cache straight into shared memory (qsa_decode: the compact row
+// never exists in device memory); Src::kCacheStore does the same and also
+// writes every row from shared memory to the scratch (qsa_gather_attend,
+// the same bytes as qsa_gather).
 #include <cstddef>
 
 #include "qsa_internal.cuh"
@@ -43,27 +50,30 @@
 namespace qsa {
 namespace {
 
-constexpr int kParts = kAttendParts;             // CTAs per (query, KV head)
-constexpr int kSC = kAttendChunk;                // rows per sub-chunk
-constexpr int kStages = 2;
-constexpr int kThreads = 256;                    // 8 warps
-constexpr int kMaxSub = (4 * QSA_MAX_BUDGET + 3 + kSC - 1) / kSC;   // 33 sub-chunks at most
-constexpr int kMaxSubPerCta = (kMaxSub + kParts - 1) / kParts;     // 5
-constexpr int kMaxRows = kMaxSubPerCta * kSC;                      // 320 rows per CTA at most
+constexpr int kRowsPerPart = kAttendRowsPerPart;
+constexpr int kParts = kAttendParts;               // 9 runs at most (2,051 rows)
+constexpr int kStepRows = 8;                       // rows per warp step
+constexpr int kRing = 3;                           // steps in flight per warp (ring slots)
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+enum class Src { kScratch, kCache, kCacheStore };
 
 template <int D, int GQ>
 struct AttendSmem {
-    static constexpr int kKStride = D + 4;       // float4 rows land on distinct banks
     // every array read or written as float4 (or by 16-byte async copies)
     // starts on a 16-byte boundary whatever GQ and D are
+    alignas(128) float k[kWarps][kRing][kStepRows][D];  // also the end-of-run reduction area
+    alignas(128) float v[kWarps][kRing][kStepRows][D];
     alignas(16) float q[GQ][D];
-    alignas(16) float k[kStages][kSC][kKStride]; // also the end-of-run reduction area
-    alignas(16) float v[kStages][kSC][D];
-    alignas(16) float x[2][GQ][kSC];             // scaled scores, double buffered
-    alignas(16) float pt[2][kSC][GQ < 4 ? 4 : GQ]; // weights, heads inner, double buffered
-    alignas(16) float alpha[2][GQ < 4 ? 4 : GQ];   // rescale factors, double buffered
-    int64_t off[kMaxRows];                       // element offset of each row in its source, -1: none
-    float m_fin[GQ], l_fin[GQ];
+    alignas(16) float pt[kWarps][kStepRows][GQ < 4 ? 4 : GQ];  // weights of a warp's step, [row][head]
+    alignas(16) float alpha[kWarps][GQ < 4 ? 4 : GQ];          // rescale factors of a warp's step
+    alignas(16) float wm[kWarps][GQ];       // warp states at the end of the run
+    alignas(16) float wl[kWarps][GQ];
+    alignas(16) float ww[kWarps][GQ];       // their merge weights
+    alignas(16) float pw[GQ][kParts];       // merge weights of the runs (last CTA)
+    int64_t off[kRowsPerPart];              // element offset of each row of the run; -1 none, -2 bad
+    float l_fin[GQ];
     int last;
 };
 
@@ -75,41 +85,56 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// 32 partial values per lane, v[t], t = 0..31 -> lane L holds sum over lanes of v[L]
-// (recursive halving: 31 shuffles).
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
+// Reduce-scatter over the DS = 2*O lanes of an xor group (offsets O, O/2, .., 1):
+// N values per lane in, max(1, N/DS) values per lane out (v[0..]).  While more
+// than one value is left, each level halves them (the lane with bit O set keeps
+// the upper half); after that it is a plain butterfly sum.
+template <int N, int O>
+__device__ __forceinline__ void reduce_scatter(float (&v)[32], int lane)
 {
+    if constexpr (O >= 1) {
+        if constexpr (N > 1) {
+            const bool upper = (lane & O) != 0;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int j = 0; j < off; ++j) {
-            const float give = upper ? v[j] : v[j + off];
-            const float keep = upper ? v[j + off] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, off);
+            for (int j = 0; j < N / 2; ++j) {
+                const float give = upper ? v[j] : v[j + N / 2];
+                const float keep = upper ? v[j + N / 2] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, give, O);
+            }
+            reduce_scatter<N / 2, O / 2>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            reduce_scatter<1, O / 2>(v, lane);
         }
     }
-    return v[0];
 }
 
-template <int D, int GQ, bool kFromCache>
+template <int D, int GQ, Src kSrc>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_kernel(const AttendArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     using Sm = AttendSmem<D, GQ>;
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
-    constexpr int F4 = D / 4;
-    constexpr int kGP = GQ < 4 ? 4 : GQ;
-    constexpr int kPerRowThreads = 4;              // threads moving one row
-    constexpr int kChunks = F4 / kPerRowThreads;   // 16-byte pieces per thread per row and matrix
+    constexpr int F4 = D / 4;                    // 16-byte columns of a row
+    constexpr int kGP = GQ < 4 ? 4 : GQ;         // padded head count of pt / alpha
+    constexpr bool kFromCache = kSrc != Src::kScratch;
+    constexpr bool kStore = kSrc == Src::kCacheStore;
+    // score layout: HP head groups x DS lanes; a lane holds HPL heads x NF columns
+    constexpr int HP = GQ < 4 ? GQ : 4;
+    constexpr int HPL = GQ / HP;
+    constexpr int DS = 32 / HP;
+    constexpr int NF = (F4 + DS - 1) / DS;
+    constexpr int NV = kStepRows * HPL;          // partial dots per lane before the reduce
+    constexpr int RSH = DS / kStepRows;          // lanes sharing a row after the reduce (>= 1)
+    static_assert(NV <= 32 && (NV >= DS ? NV / DS == HPL : HPL == 1), "one row per lane after the reduce");
 
     const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = a.q_heads / a.kv_heads;  // <= GQ
     const int h0 = kvh * gq;
 
-    // ---- independent of the previous kernel: the queries ---------------------------
+    // ---- independent of the previous kernel: queries and the history -------------
     {
         const float4 *qg = reinterpret_cast<const float4 *>(a.q + (int64_t(b) * a.q_heads + h0) * D);
         for (int e = tid; e < GQ * F4; e += kThreads) {
@@ -118,10 +143,19 @@ attend_kernel(const AttendArgs a)
                 hh < gq ? __ldg(qg + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    wait_for_predecessor();  // ids, n_ids (and the scratch) come from earlier kernels
+    const int T = kFromCache ? __ldg(a.visible + b) : 0;
+    const int64_t smap_off = kFromCache ? __ldg(a.slot_offset + b) : 0;
+    wait_for_predecessor();  // ids and n_ids (or the scratch) come from earlier kernels
 
     // n_ids and ids come from the previous kernel, which may still have been
-    // running when this one started: L2-coherent loads, never the read-only path
+    // running when this one started: L2-coherent loads, never the read-only path.
+    // The ID of this thread's row is loaded with n (one round trip) and used
+    // only if the row exists.
+    const int64_t row_base = int64_t(b) * a.row_cap;   // ids / scratch row of query b
+    const int r0 = part * kRowsPerPart;
+    const int my_r = r0 + tid;
+    int id = 0;
+    if (kFromCache && my_r < a.row_cap) id = __ldcg(a.ids + row_base + my_r);
     const int n = __ldcg(a.n_ids + b);
     if (n < 0 || n > a.row_cap) {
         if (part == 0) {
@@ -130,293 +164,313 @@ attend_kernel(const AttendArgs a)
         }
         return;
     }
-    const int nsub = (n + kSC - 1) / kSC;
-    const int per = (nsub + kParts - 1) / kParts;
-    const int s_begin = min(nsub, part * per);
-    const int s_end = min(nsub, s_begin + per);
-    const int my_sub = s_end - s_begin;
-    const int64_t row_base = int64_t(b) * a.row_cap;          // scratch / ids row of query b
-    const int64_t scr_rs = a.kv_heads;                        // scratch rows apart, in D units
-    const int r_first = s_begin * kSC;
-    const int r_last = min(n, s_end * kSC);
-    const float *ksrc = kFromCache ? a.k_cache : a.k_scr;
-    const float *vsrc = kFromCache ? a.v_cache : a.v_scr;
+    const int used = max(1, (n + kRowsPerPart - 1) / kRowsPerPart);  // runs of this query
+    if (part >= used) return;
+    const int r_end = min(n, r0 + kRowsPerPart);
+    const int64_t rs = a.kv_heads;                                   // scratch rows apart, in D units
 
-    // ---- resolve every row of this CTA once: all ID loads, then all slot loads ------
+    // ---- resolve the run: thread t takes row r0 + t ---------------------------------
     {
-        constexpr int kPer = (kMaxRows + kThreads - 1) / kThreads;  // 2
-        int id[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int r = r_first + tid + u * kThreads;
-            id[u] = (kFromCache && r < r_last) ? __ldcg(a.ids + row_base + r) : -1;
-        }
-        const int T = kFromCache ? __ldg(a.visible + b) : 0;
-        const int32_t *smap = kFromCache ? a.slot_map + __ldg(a.slot_offset + b) : nullptr;
-        int64_t slot[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int r = r_first + tid + u * kThreads;
-            slot[u] = -1;
-            if (kFromCache && r < r_last) {
-                if (id[u] >= 0 && id[u] < T) slot[u] = __ldg(smap + id[u]);
-                else set_error(a.err, QSA_DEVERR_ROW_RANGE);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int rl = tid + u * kThreads;  // row within this CTA's run
-            if (rl < kMaxRows) {
-                const int r = r_first + rl;
-                int64_t o = -1;
-                if (r < r_last) {
-                    if (kFromCache) {
-                        if (slot[u] >= 0 && slot[u] < a.num_slots) o = (slot[u] * a.kv_heads + kvh) * D;
-                        else if (id[u] >= 0 && id[u] < T) set_error(a.err, QSA_DEVERR_SLOT_RANGE);
+        int64_t o = -1;
+        if (my_r < r_end) {
+            if constexpr (kFromCache) {
+                if (id >= 0 && id < T) {
+                    const int slot = __ldg(a.slot_map + smap_off + id);
+                    if (slot >= 0 && slot < a.num_slots) {
+                        o = (int64_t(slot) * a.kv_heads + kvh) * D;
                     } else {
-                        o = ((row_base + r) * scr_rs + kvh) * D;
+                        o = -2;
+                        set_error(a.err, QSA_DEVERR_SLOT_RANGE);
                     }
+                } else {
+                    o = -2;
+                    set_error(a.err, QSA_DEVERR_ROW_RANGE);
                 }
-                sm.off[rl] = o;
+            } else {
+                o = ((row_base + my_r) * rs + kvh) * D;
             }
         }
+        sm.off[tid] = o;
     }
     __syncthreads();
 
-    // rows of sub-chunk s into stage st: thread = (row i, quarter), 16-byte async copies
-    const int mi = tid / kPerRowThreads;        // row moved by this thread
-    const int mq = tid % kPerRowThreads;        // its quarter of the row
-    auto issue = [&](int s) {
-        const int st = s % kStages;
-        const int r = (s_begin + s) * kSC + mi;
-        const int64_t o = sm.off[s * kSC + mi];
-        if (o >= 0) {
+    // ---- this warp's steps: j = warp, warp + 8, ... ---------------------------------
+    const int nsteps = (r_end - r0 + kStepRows - 1) / kStepRows;
+    const int my_steps = nsteps > warp ? (nsteps - warp + kWarps - 1) / kWarps : 0;
+    const float *ksrc = kFromCache ? a.k_cache : a.k_scr;
+    const float *vsrc = kFromCache ? a.v_cache : a.v_scr;
+    auto issue = [&](int k) {  // the warp's k-th step into ring slot k % kRing
+        const int j = warp + kWarps * k;
+        const int sl = k % kRing;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                const int j4 = mq * kChunks + c;
-                cp_async16(&sm.k[st][mi][4 * j4], ksrc + o + 4 * j4);
-                cp_async16(&sm.v[st][mi][4 * j4], vsrc + o + 4 * j4);
-            }
-        } else if (r < n) {  // unresolvable row (flagged): zeros
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                const int j4 = mq * kChunks + c;
-                *reinterpret_cast<float4 *>(&sm.k[st][mi][4 * j4]) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4 *>(&sm.v[st][mi][4 * j4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = lane; e < kStepRows * F4; e += 32) {
+            const int r = e / F4, c = e - r * F4;
+            const int rl = j * kStepRows + r;  // row within the run
+            const int64_t o = r0 + rl < r_end ? sm.off[rl] : -1;
+            if (o >= 0) {
+                cp_async16(&sm.k[warp][sl][r][4 * c], ksrc + o + 4 * c);
+                cp_async16(&sm.v[warp][sl][r][4 * c], vsrc + o + 4 * c);
+            } else if (o == -2) {  // unresolvable row (flagged): zeros
+                *reinterpret_cast<float4 *>(&sm.k[warp][sl][r][4 * c]) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(&sm.v[warp][sl][r][4 * c]) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        cp_async_commit();
     };
-    if (my_sub > 0) issue(0);
-
-    // lane = 16-byte column d4 of a row (lanes >= F4 idle in the math)
-    const bool col = lane < F4;
-    float4 qreg[GQ];
 #pragma unroll
-    for (int hh = 0; hh < GQ; ++hh)
-        qreg[hh] = col ? *reinterpret_cast<const float4 *>(&sm.q[hh][4 * lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kRing - 1; ++k) {
+        if (k < my_steps) issue(k);
+        cp_async_commit();
+    }
+
+    // score-layout coordinates of this lane
+    const int hg = lane / DS, ds = lane % DS;
+    const int r_lane = ds / RSH;                 // the row whose dots this lane ends with
+    float4 qreg[HPL][NF];
+#pragma unroll
+    for (int u = 0; u < HPL; ++u)
+#pragma unroll
+        for (int i = 0; i < NF; ++i) {
+            const int c = ds + DS * i;
+            qreg[u][i] = c < F4 ? *reinterpret_cast<const float4 *>(&sm.q[hg * HPL + u][4 * c])
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    const bool col = lane < F4;  // value layout: lane = 16-byte column (lanes >= F4 idle)
     float4 acc[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float m_run = -INFINITY, l_run = 0.0f;   // softmax state of this warp's head(s)
-    float m_run2 = -INFINITY, l_run2 = 0.0f;
-    constexpr int R = 32 / GQ;   // rows per group: R rows x GQ heads = 32 dot products
-    constexpr int NG = kSC / R;  // groups per sub-chunk
-
-    for (int s = 0; s < my_sub; ++s) {
-        const int st = s % kStages;
-        const int buf = s & 1;
-        const int r0 = (s_begin + s) * kSC;
-        const int rows = min(kSC, n - r0);
-        if (s + 1 < my_sub) {
-            issue(s + 1);        // the next sub-chunk streams in while this one is used
-            cp_async_wait<1>();  // this thread's pieces of sub-chunk s have landed
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();         // ... and everyone else's
-
-        if (kFromCache && mi < rows) {
-            // the gather's output: this KV head's slice of scratch row r0 + mi
-            float4 *kd = reinterpret_cast<float4 *>(a.k_scr_out + ((row_base + r0 + mi) * scr_rs + kvh) * D);
-            float4 *vd = reinterpret_cast<float4 *>(a.v_scr_out + ((row_base + r0 + mi) * scr_rs + kvh) * D);
+    float m_run[HPL], l_run[HPL];  // states of heads hg*HPL + u over this warp's rows
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                const int j4 = mq * kChunks + c;
-                kd[j4] = *reinterpret_cast<const float4 *>(&sm.k[st][mi][4 * j4]);
-                vd[j4] = *reinterpret_cast<const float4 *>(&sm.v[st][mi][4 * j4]);
+    for (int u = 0; u < HPL; ++u) {
+        m_run[u] = -INFINITY;
+        l_run[u] = 0.0f;
+    }
+
+    for (int k = 0; k < my_steps; ++k) {
+        if (k + kRing - 1 < my_steps) issue(k + kRing - 1);  // into the slot step k-1 used
+        cp_async_commit();
+        cp_async_wait<kRing - 1>();  // this lane's copies of step k have landed
+        __syncwarp();                // ... and the whole warp's
+        const int sl = k % kRing;
+        const int j = warp + kWarps * k;
+        const int rows = min(kStepRows, r_end - (r0 + j * kStepRows));
+
+        if constexpr (kStore) {
+            // the gather's output: the step's rows, from shared memory to the scratch
+            for (int e = lane; e < rows * F4; e += 32) {
+                const int r = e / F4, c = e - r * F4;
+                const int64_t dst = ((row_base + r0 + j * kStepRows + r) * rs + kvh) * D + 4 * c;
+                *reinterpret_cast<float4 *>(a.k_scr_out + dst) = *reinterpret_cast<const float4 *>(&sm.k[warp][sl][r][4 * c]);
+                *reinterpret_cast<float4 *>(a.v_scr_out + dst) = *reinterpret_cast<const float4 *>(&sm.v[warp][sl][r][4 * c]);
             }
         }
 
-        // ---- scaled scores: a warp takes R rows at a time, lane = column ------------
-        for (int g = warp; g < NG; g += kThreads / 32) {
-            float v[32];
+        // ---- 8 rows x HPL heads of partial dots over this lane's columns --------------
+        float v[32];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float4 kv = col ? *reinterpret_cast<const float4 *>(&sm.k[st][g * R + r][4 * lane])
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < kStepRows; ++r) {
 #pragma unroll
-                for (int hh = 0; hh < GQ; ++hh) {
-                    float d = qreg[hh].x * kv.x;
-                    d = fmaf(qreg[hh].y, kv.y, d);
-                    d = fmaf(qreg[hh].z, kv.z, d);
-                    d = fmaf(qreg[hh].w, kv.w, d);
-                    v[r * GQ + hh] = d;
+            for (int i = 0; i < NF; ++i) {
+                const int c = ds + DS * i;
+                const float4 kv = c < F4 ? *reinterpret_cast<const float4 *>(&sm.k[warp][sl][r][4 * c])
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < HPL; ++u) {
+                    float d = i == 0 ? qreg[u][i].x * kv.x : fmaf(qreg[u][i].x, kv.x, v[r * HPL + u]);
+                    d = fmaf(qreg[u][i].y, kv.y, d);
+                    d = fmaf(qreg[u][i].z, kv.z, d);
+                    d = fmaf(qreg[u][i].w, kv.w, d);
+                    v[r * HPL + u] = d;
                 }
             }
-            const float dot = reduce_scatter32(v, lane);  // lane L: row L / GQ, head L % GQ
-            const int hh = lane % GQ;
-            const int i = g * R + lane / GQ;
-            sm.x[buf][hh][i] = (i < rows && hh < gq) ? a.scale * dot : -INFINITY;
         }
-        __syncthreads();
+        reduce_scatter<NV, DS / 2>(v, lane);  // v[u]: row r_lane, head hg*HPL + u
 
-        // ---- online softmax state, one warp per head (two for 16 heads) ---------------
+        // ---- online softmax step of this lane's heads over the 8 rows ------------------
+        float al[HPL];
+        bool unit = true;  // every rescale factor is 1 (nothing to rescale)
 #pragma unroll
-        for (int rep = 0; rep < (GQ + 7) / 8; ++rep) {
-            const int hh = warp + 8 * rep;
-            if (hh < GQ) {
-                const float x0 = sm.x[buf][hh][lane], x1 = sm.x[buf][hh][lane + 32];
-                float mc = fmaxf(x0, x1);
+        for (int u = 0; u < HPL; ++u) {
+            const bool ok = r_lane < rows && hg * HPL + u < gq;
+            const float x = ok ? a.scale * v[u] : -INFINITY;
+            float mc = x;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-                float &mr = rep == 0 ? m_run : m_run2;
-                float &lr = rep == 0 ? l_run : l_run2;
-                const float m_new = fmaxf(mr, mc);
-                float p0 = 0.0f, p1 = 0.0f, al = 0.0f;
-                if (m_new != -INFINITY) {
-                    p0 = expf(x0 - m_new);
-                    p1 = expf(x1 - m_new);
-                    al = mr == -INFINITY ? 0.0f : expf(mr - m_new);
-                }
-                sm.pt[buf][lane][hh] = p0;
-                sm.pt[buf][lane + 32][hh] = p1;
-                float ps = p0 + p1;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-                lr = fmaf(lr, al, ps);
-                mr = m_new;
-                if (lane == 0) sm.alpha[buf][hh] = al;
+            for (int o = RSH; o < DS; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+            const float m_new = fmaxf(m_run[u], mc);
+            float p = 0.0f, alpha = 0.0f;
+            if (m_new != -INFINITY) {
+                p = expf(x - m_new);
+                alpha = m_run[u] == -INFINITY ? 0.0f : expf(m_run[u] - m_new);
             }
+            float ps = p;
+#pragma unroll
+            for (int o = RSH; o < DS; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            l_run[u] = fmaf(l_run[u], alpha, ps);
+            m_run[u] = m_new;
+            al[u] = alpha;
+            unit = unit && (alpha == 1.0f || m_new == -INFINITY);
+            if (ds % RSH == 0) sm.pt[warp][r_lane][hg * HPL + u] = p;
         }
-        __syncthreads();
+        if (ds == 0) {
+#pragma unroll
+            for (int u = 0; u < HPL; ++u) sm.alpha[warp][hg * HPL + u] = al[u];
+        }
+        const bool rescale = !__all_sync(0xffffffffu, unit);
+        __syncwarp();
 
-        // ---- acc[h] = acc[h] * alpha_h + sum_i p_ih v_i over this warp's 8 rows --------
+        // ---- acc[h] = acc[h] * alpha_h + sum_r p_rh v_r ---------------------------------
         if (col) {
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                const float al = sm.alpha[buf][hh];
-                acc[hh].x *= al;
-                acc[hh].y *= al;
-                acc[hh].z *= al;
-                acc[hh].w *= al;
-            }
-            const int i0 = warp * (kSC / 8);
-            const int i1 = min(rows, i0 + kSC / 8);
-            for (int i = i0; i < i1; ++i) {
-                const float4 vv = *reinterpret_cast<const float4 *>(&sm.v[st][i][4 * lane]);
+            if (rescale) {  // (multiplying by 1 would change nothing)
 #pragma unroll
                 for (int h4 = 0; h4 < kGP / 4; ++h4) {
-                    const float4 pp = *reinterpret_cast<const float4 *>(&sm.pt[buf][i][4 * h4]);
-                    const float pw[4] = {pp.x, pp.y, pp.z, pp.w};
+                    const float4 al4 = *reinterpret_cast<const float4 *>(&sm.alpha[warp][4 * h4]);
+                    const float alw[4] = {al4.x, al4.y, al4.z, al4.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int hh = 4 * h4 + u;
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const int hh = 4 * h4 + w4;
                         if (hh < GQ) {
-                            acc[hh].x = fmaf(pw[u], vv.x, acc[hh].x);
-                            acc[hh].y = fmaf(pw[u], vv.y, acc[hh].y);
-                            acc[hh].z = fmaf(pw[u], vv.z, acc[hh].z);
-                            acc[hh].w = fmaf(pw[u], vv.w, acc[hh].w);
+                            acc[hh].x *= alw[w4];
+                            acc[hh].y *= alw[w4];
+                            acc[hh].z *= alw[w4];
+                            acc[hh].w *= alw[w4];
                         }
                     }
                 }
             }
+#pragma unroll
+            for (int r = 0; r < kStepRows; ++r) {
+                if (r < rows) {
+                    const float4 vv = *reinterpret_cast<const float4 *>(&sm.v[warp][sl][r][4 * lane]);
+                    float pw[kGP];
+#pragma unroll
+                    for (int h4 = 0; h4 < kGP / 4; ++h4) {
+                        const float4 pp = *reinterpret_cast<const float4 *>(&sm.pt[warp][r][4 * h4]);
+                        pw[4 * h4 + 0] = pp.x;
+                        pw[4 * h4 + 1] = pp.y;
+                        pw[4 * h4 + 2] = pp.z;
+                        pw[4 * h4 + 3] = pp.w;
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < GQ; ++hh) {
+                        acc[hh].x = fmaf(pw[hh], vv.x, acc[hh].x);
+                        acc[hh].y = fmaf(pw[hh], vv.y, acc[hh].y);
+                        acc[hh].z = fmaf(pw[hh], vv.z, acc[hh].z);
+                        acc[hh].w = fmaf(pw[hh], vv.w, acc[hh].w);
+                    }
+                }
+            }
         }
-        __syncthreads();  // stage st may be refilled by the next iteration's copies
+        __syncwarp();  // the slot, pt and alpha are rewritten by later steps
     }
+    cp_async_wait<0>();
 
-    // ---- this CTA's partial: acc summed over the 8 warps (fixed order) --------------
-    float *red = &sm.k[0][0][0];  // [8 warps][GQ][D]; every copy has landed
+    // ---- this CTA's partial: the eight warp states merged in warp order ------------
+    __syncthreads();  // every warp is done with its ring: it becomes the reduction area
+    float *red = &sm.k[0][0][0][0];  // [kWarps][GQ][D]
     if (col) {
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh)
             *reinterpret_cast<float4 *>(&red[(warp * GQ + hh) * D + 4 * lane]) = acc[hh];
     }
-    if (lane == 0) {
+    if (ds == 0) {
 #pragma unroll
-        for (int rep = 0; rep < (GQ + 7) / 8; ++rep) {
-            const int hh = warp + 8 * rep;
-            if (hh < GQ) {
-                sm.m_fin[hh] = rep == 0 ? m_run : m_run2;
-                sm.l_fin[hh] = rep == 0 ? l_run : l_run2;
-            }
+        for (int u = 0; u < HPL; ++u) {
+            sm.wm[warp][hg * HPL + u] = m_run[u];
+            sm.wl[warp][hg * HPL + u] = l_run[u];
         }
     }
     __syncthreads();
-    const int64_t pbase = (int64_t(b) * a.q_heads + h0) * a.nparts + part;  // head h0, part
+    const int64_t pbase = (int64_t(b) * a.q_heads + h0) * a.nparts + part;  // head h0, this run
+    if (tid < gq) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][tid]);
+        float L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float wt = M == -INFINITY ? 0.0f : expf(sm.wm[w][tid] - M);
+            sm.ww[w][tid] = wt;
+            L = fmaf(sm.wl[w][tid], wt, L);
+        }
+        a.part_m[pbase + int64_t(tid) * a.nparts] = M;
+        a.part_l[pbase + int64_t(tid) * a.nparts] = L;
+    }
+    __syncthreads();
     for (int e = tid; e < gq * F4; e += kThreads) {
         const int hh = e / F4, j4 = e - hh * F4;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
             const float4 p = *reinterpret_cast<const float4 *>(&red[(w * GQ + hh) * D + 4 * j4]);
-            o.x += p.x;
-            o.y += p.y;
-            o.z += p.z;
-            o.w += p.w;
+            const float wt = sm.ww[w][hh];
+            o.x = fmaf(p.x, wt, o.x);
+            o.y = fmaf(p.y, wt, o.y);
+            o.z = fmaf(p.z, wt, o.z);
+            o.w = fmaf(p.w, wt, o.w);
         }
         reinterpret_cast<float4 *>(a.part_acc + (pbase + int64_t(hh) * a.nparts) * D)[j4] = o;
     }
-    if (tid < gq) {
-        a.part_m[pbase + int64_t(tid) * a.nparts] = sm.m_fin[tid];
-        a.part_l[pbase + int64_t(tid) * a.nparts] = sm.l_fin[tid];
-    }
 
-    // ---- the last CTA of this (query, KV head) merges the parts in order ----------
+    // ---- the last CTA of this (query, KV head) merges the runs in order ------------
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         uint32_t *ticket = a.tickets + int64_t(b) * a.kv_heads + kvh;
-        sm.last = atomicAdd(ticket, 1u) == uint32_t(kParts - 1);
+        sm.last = atomicAdd(ticket, 1u) == uint32_t(used - 1);
         if (sm.last) *ticket = 0u;  // leave the ticket clean for the next call
     }
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
     const int64_t hb0 = (int64_t(b) * a.q_heads + h0) * a.nparts;
-    // part maxima and denominators first (one round of loads), then the accumulators
-    float *wm = &sm.x[0][0][0];  // [GQ][kParts] weights, reused
-    for (int e = tid; e < gq * kParts; e += kThreads) {
-        const int hh = e / kParts, c = e - hh * kParts;
-        wm[hh * kParts + c] = __ldcg(a.part_m + hb0 + int64_t(hh) * a.nparts + c);
+    // every load first (one round trip), then the weights, then the sums
+    const int e0 = tid;  // one (head, column) element per thread when gq * F4 <= 256
+    const int hh0 = e0 / F4, jj0 = e0 - hh0 * F4;
+    float4 xv[kParts];
+    if (e0 < gq * F4) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh0) * a.nparts) * D) + jj0;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c)
+            xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
     if (tid < gq) {
-        float M = -INFINITY;
-        for (int c = 0; c < kParts; ++c) M = fmaxf(M, wm[tid * kParts + c]);
-        float L = 0.0f;
+        const int64_t hb = hb0 + int64_t(tid) * a.nparts;
+        float pm[kParts], pl[kParts];
+#pragma unroll
         for (int c = 0; c < kParts; ++c) {
-            const float w = M == -INFINITY ? 0.0f : expf(wm[tid * kParts + c] - M);
-            L = fmaf(__ldcg(a.part_l + hb0 + int64_t(tid) * a.nparts + c), w, L);
-            wm[tid * kParts + c] = w;
+            pm[c] = c < used ? __ldcg(a.part_m + hb + c) : -INFINITY;
+            pl[c] = c < used ? __ldcg(a.part_l + hb + c) : 0.0f;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) M = fmaxf(M, pm[c]);
+        float L = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) {
+            const float w = (c >= used || M == -INFINITY) ? 0.0f : expf(pm[c] - M);
+            if (c < used) L = fmaf(pl[c], w, L);
+            sm.pw[tid][c] = w;
         }
         sm.l_fin[tid] = L;
     }
     __syncthreads();
     for (int e = tid; e < gq * F4; e += kThreads) {
         const int hh = e / F4, j4 = e - hh * F4;
-        const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh) * a.nparts) * D) + j4;
-        float4 xv[kParts];
+        if (e != e0) {  // more elements than threads: load this one now
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh) * a.nparts) * D) + j4;
 #pragma unroll
-        for (int c = 0; c < kParts; ++c) xv[c] = __ldcg(src + int64_t(c) * F4);
+            for (int c = 0; c < kParts; ++c)
+                xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kParts; ++c) {
-            const float w = wm[hh * kParts + c];
-            o.x = fmaf(xv[c].x, w, o.x);
-            o.y = fmaf(xv[c].y, w, o.y);
-            o.z = fmaf(xv[c].z, w, o.z);
-            o.w = fmaf(xv[c].w, w, o.w);
+            if (c < used) {
+                const float w = sm.pw[hh][c];
+                o.x = fmaf(xv[c].x, w, o.x);
+                o.y = fmaf(xv[c].y, w, o.y);
+                o.z = fmaf(xv[c].z, w, o.z);
+                o.w = fmaf(xv[c].w, w, o.w);
+            }
         }
         const float L = sm.l_fin[hh];
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -425,7 +479,7 @@ attend_kernel(const AttendArgs a)
     }
 }
 
-template <int D, int GQ, bool kFromCache>
+template <int D, int GQ, Src kSrc>
 cudaError_t launch_attend_t(const AttendArgs &a, cudaStream_t s, bool pdl)
 {
     const size_t smem = sizeof(AttendSmem<D, GQ>);
@@ -434,42 +488,51 @@ cudaError_t launch_attend_t(const AttendArgs &a, cudaStream_t s, bool pdl)
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, GQ, kFromCache>,
+        cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, GQ, kSrc>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
     const dim3 grid(kParts, unsigned(a.kv_heads), unsigned(a.batch));
-    return launch_kernel(attend_kernel<D, GQ, kFromCache>, grid, dim3(kThreads), smem, s, pdl, a);
+    return launch_kernel(attend_kernel<D, GQ, kSrc>, grid, dim3(kThreads), smem, s, pdl, a);
 }
 
-template <int D, bool kFromCache>
+template <int D, Src kSrc>
 cudaError_t launch_attend_d(const AttendArgs &a, cudaStream_t s, bool pdl)
 {
     const int gq = a.q_heads / a.kv_heads;
-    if (gq <= 1) return launch_attend_t<D, 1, kFromCache>(a, s, pdl);
-    if (gq <= 2) return launch_attend_t<D, 2, kFromCache>(a, s, pdl);
-    if (gq <= 4) return launch_attend_t<D, 4, kFromCache>(a, s, pdl);
-    if (gq <= 8) return launch_attend_t<D, 8, kFromCache>(a, s, pdl);
-    return launch_attend_t<D, 16, kFromCache>(a, s, pdl);
+    if (gq <= 1) return launch_attend_t<D, 1, kSrc>(a, s, pdl);
+    if (gq <= 2) return launch_attend_t<D, 2, kSrc>(a, s, pdl);
+    if (gq <= 4) return launch_attend_t<D, 4, kSrc>(a, s, pdl);
+    if (gq <= 8) return launch_attend_t<D, 8, kSrc>(a, s, pdl);
+    return launch_attend_t<D, 16, kSrc>(a, s, pdl);
+}
+
+template <int D>
+cudaError_t launch_attend_src(const AttendArgs &a, cudaStream_t s, bool pdl)
+{
+    if (a.k_cache == nullptr) return launch_attend_d<D, Src::kScratch>(a, s, pdl);
+    if (a.k_scr_out == nullptr) return launch_attend_d<D, Src::kCache>(a, s, pdl);
+    return launch_attend_d<D, Src::kCacheStore>(a, s, pdl);
 }
 
 static_assert(sizeof(AttendSmem<128, 16>) <= 227 * 1024, "shared memory per CTA");
-static_assert(kThreads / 32 == 8, "the end-of-run reduction sums 8 warps; P.V takes 8 rows per warp");
+static_assert(kRowsPerPart == kThreads, "one thread per row of the run resolves it");
+static_assert(kParts * kRowsPerPart >= kGroup * QSA_MAX_BUDGET + kGroup - 1, "runs cover the longest row");
+static_assert(kRowsPerPart % kStepRows == 0, "runs are whole steps");
 
 template <int D, int GQ>
 constexpr bool layout_ok()
 {
     using S = AttendSmem<D, GQ>;
-    return offsetof(S, q) % 16 == 0 && offsetof(S, k) % 16 == 0 && offsetof(S, v) % 16 == 0 &&
-           offsetof(S, x) % 16 == 0 && offsetof(S, pt) % 16 == 0 && offsetof(S, alpha) % 16 == 0 &&
-           offsetof(S, off) % 8 == 0 && (S::kKStride * 4) % 16 == 0 && sizeof(S::x) >= GQ * kParts * 4 &&
-           sizeof(S::k) >= size_t(8) * GQ * D * 4;  // room for the end-of-run reduction
+    return offsetof(S, k) % 16 == 0 && offsetof(S, v) % 16 == 0 && offsetof(S, q) % 16 == 0 &&
+           offsetof(S, pt) % 16 == 0 && offsetof(S, alpha) % 16 == 0 && offsetof(S, off) % 8 == 0 &&
+           (D * 4) % 16 == 0 && sizeof(S::k) >= size_t(kWarps) * GQ * D * 4;  // room for the reduction
 }
 static_assert(layout_ok<64, 1>() && layout_ok<64, 2>() && layout_ok<64, 4>() && layout_ok<64, 8>() &&
                   layout_ok<64, 16>() && layout_ok<128, 1>() && layout_ok<128, 2>() && layout_ok<128, 4>() &&
                   layout_ok<128, 8>() && layout_ok<128, 16>(),
-              "16-byte alignment of every float4 / bulk-copy array");
+              "16-byte alignment of every float4 / async-copy array");
 
 }  // namespace
 
@@ -483,11 +546,8 @@ bool attend_shape_supported(int head_dim, int q_heads, int kv_heads)
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl)
 {
     if (a.batch == 0) return cudaSuccess;
-    const bool fused = a.k_cache != nullptr;
-    if (a.head_dim == 128)
-        return fused ? launch_attend_d<128, true>(a, s, pdl) : launch_attend_d<128, false>(a, s, pdl);
-    if (a.head_dim == 64)
-        return fused ? launch_attend_d<64, true>(a, s, pdl) : launch_attend_d<64, false>(a, s, pdl);
+    if (a.head_dim == 128) return launch_attend_src<128>(a, s, pdl);
+    if (a.head_dim == 64) return launch_attend_src<64>(a, s, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -17,9 +17,9 @@ namespace qsa {
 // ---- workspace layout -----------------------------------------------------
 
 constexpr int kGroup = 4;            // tokens per scored group
-constexpr int kAttendChunk = 64;     // rows per attention sub-chunk
-constexpr int kAttendParts = 8;      // attention CTAs (and partials) per (query, KV head);
-                                     // the split depends on the row length only
+constexpr int kAttendRowsPerPart = 256;  // emitted rows per attention CTA
+constexpr int kAttendParts =             // attention CTAs (and partials) per (query, KV head) at
+    (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 9
 constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
 constexpr size_t kWsAlign = 256;
 
@@ -50,7 +50,7 @@ struct Layout {
     int32_t row_cap;        // IDs per row: 4*budget + 3
     int32_t nparts;         // attention partials per (query, head): kAttendParts
     size_t off_err, off_tickets, off_part_m, off_part_l, off_part_acc;
-    size_t off_qmax, off_scores, off_kscr, off_vscr;
+    size_t off_qmax, off_scores;
     size_t total;
 };
 
@@ -115,7 +115,8 @@ struct AttendArgs {
     float scale;
     uint32_t *err;
     // fused gather: when k_cache != nullptr, rows are resolved through the slot
-    // map, copied from the cache, and also written to k_scr_out / v_scr_out
+    // map and copied from the cache; when k_scr_out != nullptr they are also
+    // written to k_scr_out / v_scr_out (the gather's output)
     const int32_t *ids;
     const int32_t *visible;
     const int32_t *slot_map;
@@ -199,6 +200,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // One-dimensional bulk copy global -> shared, completing on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -208,6 +214,27 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// One-dimensional bulk copy shared -> global in this thread's bulk async-group.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2g(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed their writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's generic-proxy writes to shared memory before later
+// async-proxy (bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Programmatic dependent launch: a kernel launched with the programmatic
