@@ -24,15 +24,17 @@
 //     maximum satisfies #(key >= L) >= k, i.e. L <= s*; any smaller L works
 //     too, so only its 10 leading bits are searched for.
 //  2. Only quads whose maximum is >= L can hold keys >= L: their four scores
-//     are re-read and the keys >= L (typically ~1% of G) are compacted, in
-//     ascending position, into shared memory.
+//     are re-read and the keys >= L (typically ~1% of G) are gathered, in no
+//     particular order, into shared memory.
 //  3. s* is found among those candidates -- one per thread, 5 bits per step,
 //     all 32 values of the next digit tested at once (radix passes over
-//     12-bit digits of (key - L) when there are more than 1024) -- and the
-//     emission places them with one ordered scan.
+//     12-bit digits of (key - L) when there are more than 1024).
+//  4. Membership goes into two group bitmaps, key > s* and key == s*; one
+//     ballot / prefix-sum pass over the bitmap words then gives every member
+//     its slot in ascending position, the tie rule included.
 // When the candidates do not fit in shared memory (e.g. when everything
-// ties) the CTA takes the plain path -- the same radix select and emission
-// over all G keys read from the scores.
+// ties) the CTA takes the plain path -- the same radix select and an ordered
+// emission over all G keys read from the scores.
 // Below budget (G <= budget) every group is chosen and the row is 0..T-1.
 #include "qsa_internal.cuh"
 
@@ -44,19 +46,22 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBits = 12;           // radix digit width
 constexpr int kBins = 1 << kBits;
 constexpr int kCandCap = 8192;      // candidates (key, group) held in shared memory
-constexpr int kQuadCap = 2048;      // flagged quads held in shared memory
 constexpr int kMaxQpt = 16;         // quads per super-block held in registers
+constexpr int kMapWords = kMaxQpt * kThreads * 4 / 32;  // group bitmap words of the narrowed path
+constexpr int kFlagRegs = 4;        // flagged quads a thread loads at once
 
 struct SelSmem {
     uint32_t hist[kBins];
     uint32_t cand_key[kCandCap];
     int32_t cand_g[kCandCap];
-    int32_t qlist[kQuadCap];
-    uint32_t cnt[kMaxQpt * kWarps];
+    uint32_t map_gt[kMapWords];  // members with key > s*
+    uint32_t map_eq[kMapWords];  // groups with key == s*
     uint64_t warp_tmp[kWarps];
     uint32_t red[kWarps];
-    uint32_t mh[33];
-    uint32_t found_digit, found_above, digit;
+    uint32_t red_hi[kWarps], red_lo[kWarps];
+    uint32_t mh[3][33];          // rotating histograms of the one-per-thread search
+    uint32_t n_cand;
+    uint32_t found_digit, found_above;
 };
 
 // Block-wide exclusive scan of a 64-bit value; *total receives the sum.
@@ -172,6 +177,10 @@ __device__ __forceinline__ void kth_largest(KeyAt key_at, int n, uint32_t k, uin
 // the largest w whose count still reaches k.  After max_steps steps the
 // undecided low bits stay 0, so thr is a lower bound of the k-th largest key;
 // when every bit is decided it is exact and need = k - #(key > thr).
+// One barrier per step: step s fills histogram s mod 3 and clears (s+2) mod 3
+// (whose last readers passed this step's barrier), and every warp derives the
+// digit itself.  The three histograms are zero on entry, and again once the
+// caller has passed one more barrier after the return.
 __device__ __forceinline__ bool kth_largest_1pt(bool valid, uint32_t key, uint32_t k, uint32_t lo, uint32_t hi,
                                                 int max_steps, SelSmem &sm, uint32_t &thr, uint32_t &need)
 {
@@ -180,37 +189,36 @@ __device__ __forceinline__ bool kth_largest_1pt(bool valid, uint32_t key, uint32
     const uint32_t range = hi - lo;
     int nb = range == 0 ? 0 : 32 - __clz(range);
     uint32_t prefix = 0;
-    if (tid < 33) sm.mh[tid] = 0;
-    __syncthreads();
-    for (int steps = 0; nb > 0 && steps < max_steps; ++steps) {
+    int steps = 0;
+    for (; nb > 0 && steps < max_steps; ++steps) {
+        uint32_t *h = sm.mh[steps % 3];
         const int step = min(5, nb);
         const int shift = nb - step;
         const uint32_t ncand = 1u << step;
         uint32_t m = 0;
         if (valid && off >= prefix) m = min(ncand, ((off - prefix) >> shift) + 1u);
         const uint32_t peers = __match_any_sync(0xffffffffu, m);
-        if (m != 0 && lane == __ffs(peers) - 1) atomicAdd(&sm.mh[m], uint32_t(__popc(peers)));
+        if (m != 0 && lane == __ffs(peers) - 1) atomicAdd(&h[m], uint32_t(__popc(peers)));
         __syncthreads();
-        if (tid < 32) {
-            // count(w) = #(m > w) = sum of mh[w+1..32]: a suffix sum over the lanes
-            uint32_t c = sm.mh[lane + 1];
+        // count(w) = #(m > w) = sum of h[w+1..32]: a suffix sum over the lanes
+        uint32_t c = h[lane + 1];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xffffffffu, c, o);
-                if (lane + o < 32) c += y;
-            }
-            const uint32_t ok = __ballot_sync(0xffffffffu, uint32_t(lane) < ncand && c >= k);
-            if (lane == 0) sm.digit = 31 - __clz(ok);  // bit 0 is always set: count(0) >= k
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, c, o);
+            if (lane + o < 32) c += y;
         }
-        __syncthreads();
-        prefix += sm.digit << shift;
+        const uint32_t ok = __ballot_sync(0xffffffffu, uint32_t(lane) < ncand && c >= k);
+        const uint32_t digit = 31 - __clz(ok);  // bit 0 is always set: count(0) >= k
+        if (tid < 33) sm.mh[(steps + 2) % 3][tid] = 0;
+        prefix += digit << shift;
         nb = shift;
-        if (tid < 33) sm.mh[tid] = 0;
-        __syncthreads();
     }
     thr = lo + prefix;
-    if (nb != 0) return false;
-    need = k - uint32_t(__syncthreads_count(valid && off > prefix));
+    const bool exact = nb == 0;
+    const uint32_t above = uint32_t(__syncthreads_count(valid && off > prefix));
+    if (steps > 0 && tid < 33) sm.mh[(steps - 1) % 3][tid] = 0;  // the last step's histogram
+    if (!exact) return false;
+    need = k - above;
     return true;
 }
 
@@ -278,6 +286,15 @@ select_emit_kernel(const SelectArgs a)
                              // this kernel may start before that one ends, so what it wrote is
                              // read with L2-coherent loads (__ldcg), never the read-only path
 
+    // The quad maxima left by this call's scorer do not depend on T for their
+    // address: load them together with T (one round trip instead of two).
+    const uint32_t *qmg = a.qmax != nullptr ? a.qmax + int64_t(b) * a.qmax_stride : nullptr;
+    uint32_t qv[kMaxQpt];
+#pragma unroll
+    for (int j = 0; j < kMaxQpt; ++j) {
+        const int q = tid + j * kThreads;
+        qv[j] = (qmg != nullptr && q < a.qmax_stride) ? __ldcg(qmg + q) : 0u;
+    }
     const int T = __ldg(a.visible + b);
     int32_t *row = a.ids + int64_t(b) * a.row_cap;
     if (T < 0 || T > a.max_visible) {
@@ -299,133 +316,174 @@ select_emit_kernel(const SelectArgs a)
 
     const float *sc = a.scores + int64_t(b) * a.score_stride;
     auto key_all = [&](int i) -> uint32_t { return order_key(__ldcg(sc + i)); };
-    bool done = false;
+    bool done = false;  // (uniform across the CTA)
 
-    // ---- narrowed path: quad maxima -> L <= s* -> candidates -> s* -> emission -----
+    // ---- narrowed path: quad maxima -> L <= s* -> candidates -> s* -> bitmap -------
     // Super-block t = the quads t, t + 1024, t + 2048, ... (any partition into
     // disjoint non-empty blocks gives the bound); loads stay coalesced.
     const int nq = (G + 3) / 4;                       // quads of groups
     const int qpt = (nq + kThreads - 1) / kThreads;   // quads per super-block
     const int nsb = min(nq, kThreads);                // non-empty super-blocks
     if (nsb >= k && qpt <= kMaxQpt) {
-        const uint32_t *qmg = a.qmax != nullptr ? a.qmax + int64_t(b) * a.qmax_stride : nullptr;
-        uint32_t qv[kMaxQpt];
+        const int lane = tid & 31, warp = tid >> 5;
+        const int nwords = (G + 31) / 32;
+        for (int i = tid; i < nwords; i += kThreads) {
+            sm.map_gt[i] = 0u;
+            sm.map_eq[i] = 0u;
+        }
+        if (tid < 3 * 33) sm.mh[tid / 33][tid % 33] = 0u;
+        if (tid == 0) sm.n_cand = 0u;
 #pragma unroll
         for (int j = 0; j < kMaxQpt; ++j) {
             const int q = tid + j * kThreads;
-            qv[j] = 0;
-            if (j < qpt && q < nq) {
-                if (qmg != nullptr) {
-                    qv[j] = __ldcg(qmg + q);  // left by this call's scorer
-                } else {
-                    const float4 s4 = __ldcg(reinterpret_cast<const float4 *>(sc + 4 * q));
-                    uint32_t m = order_key(s4.x);
-                    if (4 * q + 1 < G) m = max(m, order_key(s4.y));
-                    if (4 * q + 2 < G) m = max(m, order_key(s4.z));
-                    if (4 * q + 3 < G) m = max(m, order_key(s4.w));
-                    qv[j] = m;
-                }
+            if (!(j < qpt && q < nq)) {
+                qv[j] = 0;
+            } else if (qmg == nullptr) {  // no hint: the quad maxima from the scores
+                const float4 s4 = __ldcg(reinterpret_cast<const float4 *>(sc + 4 * q));
+                uint32_t m = order_key(s4.x);
+                if (4 * q + 1 < G) m = max(m, order_key(s4.y));
+                if (4 * q + 2 < G) m = max(m, order_key(s4.z));
+                if (4 * q + 3 < G) m = max(m, order_key(s4.w));
+                qv[j] = m;
             }
         }
         uint32_t sbmax = 0;
 #pragma unroll
         for (int j = 0; j < kMaxQpt; ++j) sbmax = max(sbmax, qv[j]);
         const bool has_sb = tid < nsb;
-        const uint32_t hi = block_max(sbmax, sm);
-        const uint32_t lo = block_min(has_sb ? sbmax : 0xffffffffu, sm);
+        // range of the super-block maxima: one barrier
+        {
+            const uint32_t wmx = __reduce_max_sync(0xffffffffu, sbmax);
+            const uint32_t wmn = __reduce_min_sync(0xffffffffu, has_sb ? sbmax : 0xffffffffu);
+            if (lane == 0) {
+                sm.red_hi[warp] = wmx;
+                sm.red_lo[warp] = wmn;
+            }
+        }
+        __syncthreads();
+        const uint32_t hi = __reduce_max_sync(0xffffffffu, sm.red_hi[lane]);
+        const uint32_t lo = __reduce_min_sync(0xffffffffu, sm.red_lo[lane]);
         // L: the 10 leading bits of the k-th largest super-block maximum, the rest 0
         uint32_t L, needL;
         (void)kth_largest_1pt(has_sb, sbmax, uint32_t(k), lo, hi, 2, sm, L, needL);
 
-        // quads reaching L, in ascending order: round j holds quads 1024j..1024j+1023,
-        // so (round, warp, lane) order is quad order
-        const int lane = tid & 31, warp = tid >> 5;
-        uint32_t ball[kMaxQpt];
-        uint32_t my_cnt = 0;
+        // Candidates: the groups with key >= L of the quads whose maximum
+        // reaches L, gathered into shared memory in any order.  A thread
+        // loads up to kFlagRegs flagged quads at once (one round trip; more
+        // only when it holds more flagged quads than that).
+        uint32_t flagged = 0;  // bit j: quad tid + 1024 j reaches L
 #pragma unroll
-        for (int j = 0; j < kMaxQpt; ++j) {
-            ball[j] = __ballot_sync(0xffffffffu, qv[j] >= L && j < qpt && tid + j * kThreads < nq);
-            if (lane == 0 && j < qpt) sm.cnt[j * kWarps + warp] = __popc(ball[j]);
-        }
-        __syncthreads();
-        if (tid < qpt * kWarps) my_cnt = sm.cnt[tid];
-        uint64_t nflag;
-        const uint64_t my_off = block_excl_scan(my_cnt, sm, &nflag);
-        if (tid < qpt * kWarps) sm.cnt[tid] = uint32_t(my_off);
-        __syncthreads();
-        if (nflag <= uint64_t(kQuadCap)) {
-            const uint32_t lt_mask = (1u << lane) - 1u;
+        for (int j = 0; j < kMaxQpt; ++j)
+            if (j < qpt && tid + j * kThreads < nq && qv[j] >= L) flagged |= 1u << j;
+        while (__syncthreads_or(flagged != 0u)) {
+            int qs[kFlagRegs];
+            float4 sv[kFlagRegs];
 #pragma unroll
-            for (int j = 0; j < kMaxQpt; ++j)
-                if ((ball[j] >> lane) & 1u)
-                    sm.qlist[sm.cnt[j * kWarps + warp] + __popc(ball[j] & lt_mask)] = tid + j * kThreads;
-            __syncthreads();
-            // their groups with key >= L, in ascending position
-            uint64_t n_c = 0;
-            for (int base = 0; base < int(nflag); base += kThreads) {
-                const int e = base + tid;
-                uint32_t kk[4] = {0, 0, 0, 0};
-                int g0 = 0, nc = 0;
-                if (e < int(nflag)) {
-                    g0 = 4 * sm.qlist[e];
-                    const float4 s4 = __ldcg(reinterpret_cast<const float4 *>(sc + g0));
-                    const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        kk[u] = order_key(sv[u]);
-                        nc += (g0 + u < G) && kk[u] >= L;
-                    }
+            for (int f = 0; f < kFlagRegs; ++f) {
+                qs[f] = -1;
+                if (flagged != 0u) {
+                    const int j = __ffs(flagged) - 1;
+                    flagged &= flagged - 1u;
+                    qs[f] = tid + j * kThreads;
                 }
-                uint64_t round_total;
-                uint64_t pos = n_c + block_excl_scan(uint64_t(nc), sm, &round_total);
+            }
+#pragma unroll
+            for (int f = 0; f < kFlagRegs; ++f)
+                sv[f] = qs[f] >= 0 ? __ldcg(reinterpret_cast<const float4 *>(sc + 4 * qs[f]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            // one slot reservation per warp for all of its candidates of this round
+            uint32_t keys[kFlagRegs][4], bals[kFlagRegs][4];
+            uint32_t wtotal = 0;
+#pragma unroll
+            for (int f = 0; f < kFlagRegs; ++f) {
+                const float vals[4] = {sv[f].x, sv[f].y, sv[f].z, sv[f].w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    if (e < int(nflag) && g0 + u < G && kk[u] >= L) {
-                        if (pos < uint64_t(kCandCap)) {
-                            sm.cand_key[pos] = kk[u];
-                            sm.cand_g[pos] = g0 + u;
-                        }
-                        ++pos;
-                    }
+                    keys[f][u] = order_key(vals[u]);
+                    const bool c = qs[f] >= 0 && 4 * qs[f] + u < G && keys[f][u] >= L;
+                    bals[f][u] = __ballot_sync(0xffffffffu, c);
+                    wtotal += __popc(bals[f][u]);
                 }
-                n_c += round_total;
+            }
+            uint32_t base = 0;
+            if (lane == 0 && wtotal != 0u) base = atomicAdd(&sm.n_cand, wtotal);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int f = 0; f < kFlagRegs; ++f) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t slot = base + __popc(bals[f][u] & lt);
+                    if (((bals[f][u] >> lane) & 1u) && slot < uint32_t(kCandCap)) {
+                        sm.cand_key[slot] = keys[f][u];
+                        sm.cand_g[slot] = 4 * qs[f] + u;
+                    }
+                    base += __popc(bals[f][u]);
+                }
+            }
+        }
+        const uint32_t n_c = sm.n_cand;  // the loop's last barrier published it
+        if (n_c >= uint32_t(k) && n_c <= uint32_t(kCandCap)) {
+            const int n = int(n_c);
+            uint32_t thr, need;
+            if (n <= kThreads) {
+                const bool have = tid < n;
+                (void)kth_largest_1pt(have, have ? sm.cand_key[tid] : 0u, uint32_t(k), L, hi, 32, sm, thr, need);
+            } else {
+                kth_largest([&](int i) { return sm.cand_key[i]; }, n, uint32_t(k), L, hi, sm, thr, need);
+            }
+            // membership bitmaps
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t key = sm.cand_key[i];
+                const int g = sm.cand_g[i];
+                if (key > thr) atomicOr(&sm.map_gt[g >> 5], 1u << (g & 31));
+                else if (key == thr) atomicOr(&sm.map_eq[g >> 5], 1u << (g & 31));
             }
             __syncthreads();
-            if (n_c >= uint64_t(k) && n_c <= uint64_t(kThreads)) {
-                // one candidate per thread: bit search, then a single ordered scan
-                const int n = int(n_c);
-                const bool have = tid < n;
-                const uint32_t key = have ? sm.cand_key[tid] : 0u;
-                uint32_t thr, need;
-                (void)kth_largest_1pt(have, key, uint32_t(k), L, hi, 32, sm, thr, need);
-                const bool is_gt = have && key > thr, is_eq = have && key == thr;
-                uint64_t tot;
-                const uint64_t before = block_excl_scan((uint64_t(is_eq) << 32) | uint64_t(is_gt), sm, &tot);
-                const uint32_t gt_b = uint32_t(before), eq_b = uint32_t(before >> 32);
-                int pos = -1;
-                if (is_gt) pos = int(gt_b + min(need, eq_b));
-                else if (is_eq && eq_b < need) pos = int(gt_b + eq_b);
-                if (pos >= k) {
-                    set_error(a.err, QSA_DEVERR_ROW_RANGE);
-                    pos = -1;
-                }
-                if (pos >= 0) {
-                    const int g = sm.cand_g[tid];
-                    int32_t *o = row + kGroup * pos;
-                    o[0] = kGroup * g;
-                    o[1] = kGroup * g + 1;
-                    o[2] = kGroup * g + 2;
-                    o[3] = kGroup * g + 3;
-                }
-                done = true;
-            } else if (n_c >= uint64_t(k) && n_c <= uint64_t(kCandCap)) {
-                const int n = int(n_c);
-                uint32_t thr, need;
-                kth_largest([&](int i) { return sm.cand_key[i]; }, n, uint32_t(k), L, hi, sm, thr, need);
-                emit_in_order([&](int i) { return sm.cand_key[i]; }, [&](int i) { return sm.cand_g[i]; }, n, thr,
-                              need, k, row, a.err, sm);
-                done = true;
+            // ordered emission: thread t takes the words of groups 64t .. 64t+63
+            constexpr int WPT = kMapWords / kThreads;  // 2
+            uint32_t wg[WPT], we[WPT], n_gt = 0, n_eq = 0;
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) {
+                const int wi = WPT * tid + w;
+                wg[w] = wi < nwords ? sm.map_gt[wi] : 0u;
+                we[w] = wi < nwords ? sm.map_eq[wi] : 0u;
+                n_gt += __popc(wg[w]);
+                n_eq += __popc(we[w]);
             }
+            uint64_t tot;
+            const uint64_t before = block_excl_scan((uint64_t(n_eq) << 32) | n_gt, sm, &tot);
+            uint32_t gt_c = uint32_t(before), eq_c = uint32_t(before >> 32);
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) {
+                uint32_t bits = wg[w] | we[w];
+                while (bits != 0u) {
+                    const int bpos = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    const uint32_t bit = 1u << bpos;
+                    int pos = -1;
+                    if (wg[w] & bit) {
+                        pos = int(gt_c + min(need, eq_c));
+                        ++gt_c;
+                    } else {
+                        if (eq_c < need) pos = int(gt_c + eq_c);
+                        ++eq_c;
+                    }
+                    if (pos >= k) {  // cannot happen for a correct threshold; never write past the row
+                        set_error(a.err, QSA_DEVERR_ROW_RANGE);
+                        pos = -1;
+                    }
+                    if (pos >= 0) {
+                        const int g = 32 * (WPT * tid + w) + bpos;
+                        int32_t *o = row + kGroup * pos;
+                        o[0] = kGroup * g;
+                        o[1] = kGroup * g + 1;
+                        o[2] = kGroup * g + 2;
+                        o[3] = kGroup * g + 3;
+                    }
+                }
+            }
+            done = true;
         }
     }
 
