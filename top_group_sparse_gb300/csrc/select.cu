@@ -48,7 +48,7 @@ constexpr int kBins = 1 << kBits;
 constexpr int kCandCap = 8192;      // candidates (key, group) held in shared memory
 constexpr int kMaxQpt = 16;         // quads per super-block held in registers
 constexpr int kMapWords = kMaxQpt * kThreads * 4 / 32;  // group bitmap words of the narrowed path
-constexpr int kFlagRegs = 4;        // flagged quads a thread loads at once
+constexpr int kQuadCap = 2048;      // flagged quads listed in shared memory
 
 struct SelSmem {
     uint32_t hist[kBins];
@@ -56,11 +56,12 @@ struct SelSmem {
     int32_t cand_g[kCandCap];
     uint32_t map_gt[kMapWords];  // members with key > s*
     uint32_t map_eq[kMapWords];  // groups with key == s*
+    int32_t qlist[kQuadCap];     // flagged quads, in no particular order
     uint64_t warp_tmp[kWarps];
     uint32_t red[kWarps];
     uint32_t red_hi[kWarps], red_lo[kWarps];
     uint32_t mh[3][33];          // rotating histograms of the one-per-thread search
-    uint32_t n_cand;
+    uint32_t n_cand, n_quad;
     uint32_t found_digit, found_above;
 };
 
@@ -332,7 +333,10 @@ select_emit_kernel(const SelectArgs a)
             sm.map_eq[i] = 0u;
         }
         if (tid < 3 * 33) sm.mh[tid / 33][tid % 33] = 0u;
-        if (tid == 0) sm.n_cand = 0u;
+        if (tid == 0) {
+            sm.n_cand = 0u;
+            sm.n_quad = 0u;
+        }
 #pragma unroll
         for (int j = 0; j < kMaxQpt; ++j) {
             const int q = tid + j * kThreads;
@@ -368,61 +372,74 @@ select_emit_kernel(const SelectArgs a)
         (void)kth_largest_1pt(has_sb, sbmax, uint32_t(k), lo, hi, 2, sm, L, needL);
 
         // Candidates: the groups with key >= L of the quads whose maximum
-        // reaches L, gathered into shared memory in any order.  A thread
-        // loads up to kFlagRegs flagged quads at once (one round trip; more
-        // only when it holds more flagged quads than that).
-        uint32_t flagged = 0;  // bit j: quad tid + 1024 j reaches L
+        // reaches L, gathered into shared memory in any order.  The flagged
+        // quads are listed first (one slot reservation per warp), so that
+        // their scores then take a single round of loads, at most
+        // kQuadCap / 1024 per thread.
+        const uint32_t lt = (1u << lane) - 1u;
+        {
+            uint32_t bals[kMaxQpt], wtotal = 0;
 #pragma unroll
-        for (int j = 0; j < kMaxQpt; ++j)
-            if (j < qpt && tid + j * kThreads < nq && qv[j] >= L) flagged |= 1u << j;
-        while (__syncthreads_or(flagged != 0u)) {
-            int qs[kFlagRegs];
-            float4 sv[kFlagRegs];
+            for (int j = 0; j < kMaxQpt; ++j) {
+                bals[j] = __ballot_sync(0xffffffffu, j < qpt && tid + j * kThreads < nq && qv[j] >= L);
+                wtotal += __popc(bals[j]);
+            }
+            uint32_t base = 0;
+            if (lane == 0 && wtotal != 0u) base = atomicAdd(&sm.n_quad, wtotal);
+            base = __shfl_sync(0xffffffffu, base, 0);
 #pragma unroll
-            for (int f = 0; f < kFlagRegs; ++f) {
-                qs[f] = -1;
-                if (flagged != 0u) {
-                    const int j = __ffs(flagged) - 1;
-                    flagged &= flagged - 1u;
-                    qs[f] = tid + j * kThreads;
-                }
+            for (int j = 0; j < kMaxQpt; ++j) {
+                const uint32_t slot = base + __popc(bals[j] & lt);
+                if (((bals[j] >> lane) & 1u) && slot < uint32_t(kQuadCap)) sm.qlist[slot] = tid + j * kThreads;
+                base += __popc(bals[j]);
+            }
+        }
+        __syncthreads();
+        const uint32_t n_flag = sm.n_quad;
+        if (n_flag <= uint32_t(kQuadCap)) {
+            constexpr int kPer = kQuadCap / kThreads;  // 2
+            int qs[kPer];
+            float4 sv[kPer];
+#pragma unroll
+            for (int f = 0; f < kPer; ++f) {
+                const int e = tid + f * kThreads;
+                qs[f] = e < int(n_flag) ? sm.qlist[e] : -1;
             }
 #pragma unroll
-            for (int f = 0; f < kFlagRegs; ++f)
+            for (int f = 0; f < kPer; ++f)
                 sv[f] = qs[f] >= 0 ? __ldcg(reinterpret_cast<const float4 *>(sc + 4 * qs[f]))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-            // one slot reservation per warp for all of its candidates of this round
-            uint32_t keys[kFlagRegs][4], bals[kFlagRegs][4];
-            uint32_t wtotal = 0;
+            uint32_t keys[kPer][4], cb[kPer][4], wtotal = 0;
 #pragma unroll
-            for (int f = 0; f < kFlagRegs; ++f) {
+            for (int f = 0; f < kPer; ++f) {
                 const float vals[4] = {sv[f].x, sv[f].y, sv[f].z, sv[f].w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     keys[f][u] = order_key(vals[u]);
-                    const bool c = qs[f] >= 0 && 4 * qs[f] + u < G && keys[f][u] >= L;
-                    bals[f][u] = __ballot_sync(0xffffffffu, c);
-                    wtotal += __popc(bals[f][u]);
+                    cb[f][u] = __ballot_sync(0xffffffffu, qs[f] >= 0 && 4 * qs[f] + u < G && keys[f][u] >= L);
+                    wtotal += __popc(cb[f][u]);
                 }
             }
             uint32_t base = 0;
             if (lane == 0 && wtotal != 0u) base = atomicAdd(&sm.n_cand, wtotal);
             base = __shfl_sync(0xffffffffu, base, 0);
-            const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-            for (int f = 0; f < kFlagRegs; ++f) {
+            for (int f = 0; f < kPer; ++f) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const uint32_t slot = base + __popc(bals[f][u] & lt);
-                    if (((bals[f][u] >> lane) & 1u) && slot < uint32_t(kCandCap)) {
+                    const uint32_t slot = base + __popc(cb[f][u] & lt);
+                    if (((cb[f][u] >> lane) & 1u) && slot < uint32_t(kCandCap)) {
                         sm.cand_key[slot] = keys[f][u];
                         sm.cand_g[slot] = 4 * qs[f] + u;
                     }
-                    base += __popc(bals[f][u]);
+                    base += __popc(cb[f][u]);
                 }
             }
+        } else if (tid == 0) {
+            sm.n_cand = 0u;  // too many flagged quads: the plain path below
         }
-        const uint32_t n_c = sm.n_cand;  // the loop's last barrier published it
+        __syncthreads();
+        const uint32_t n_c = sm.n_cand;  // published by the barrier above
         if (n_c >= uint32_t(k) && n_c <= uint32_t(kCandCap)) {
             const int n = int(n_c);
             uint32_t thr, need;
