@@ -53,8 +53,8 @@ namespace {
 constexpr int kRowsPerPart = kAttendRowsPerPart;
 constexpr int kParts = kAttendParts;               // 9 runs at most (2,051 rows)
 constexpr int kStepRows = 8;                       // rows per warp step
-constexpr int kRing = 3;                           // steps in flight per warp (ring slots)
-constexpr int kWarps = 8;
+constexpr int kRing = 2;                           // steps in flight per warp (ring slots)
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 
 enum class Src { kScratch, kCache, kCacheStore };
@@ -155,7 +155,7 @@ attend_kernel(const AttendArgs a)
     const int r0 = part * kRowsPerPart;
     const int my_r = r0 + tid;
     int id = 0;
-    if (kFromCache && my_r < a.row_cap) id = __ldcg(a.ids + row_base + my_r);
+    if (kFromCache && tid < kRowsPerPart && my_r < a.row_cap) id = __ldcg(a.ids + row_base + my_r);
     const int n = __ldcg(a.n_ids + b);
     if (n < 0 || n > a.row_cap) {
         if (part == 0) {
@@ -172,7 +172,7 @@ attend_kernel(const AttendArgs a)
     // ---- resolve the run: thread t takes row r0 + t ---------------------------------
     {
         int64_t o = -1;
-        if (my_r < r_end) {
+        if (tid < kRowsPerPart && my_r < r_end) {
             if constexpr (kFromCache) {
                 if (id >= 0 && id < T) {
                     const int slot = __ldg(a.slot_map + smap_off + id);
@@ -190,7 +190,7 @@ attend_kernel(const AttendArgs a)
                 o = ((row_base + my_r) * rs + kvh) * D;
             }
         }
-        sm.off[tid] = o;
+        if (tid < kRowsPerPart) sm.off[tid] = o;
     }
     __syncthreads();
 
@@ -517,7 +517,7 @@ cudaError_t launch_attend_src(const AttendArgs &a, cudaStream_t s, bool pdl)
 }
 
 static_assert(sizeof(AttendSmem<128, 16>) <= 227 * 1024, "shared memory per CTA");
-static_assert(kRowsPerPart == kThreads, "one thread per row of the run resolves it");
+static_assert(kRowsPerPart <= kThreads, "one thread per row of the run resolves it");
 static_assert(kParts * kRowsPerPart >= kGroup * QSA_MAX_BUDGET + kGroup - 1, "runs cover the longest row");
 static_assert(kRowsPerPart % kStepRows == 0, "runs are whole steps");
 
