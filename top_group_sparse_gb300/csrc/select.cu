@@ -30,8 +30,9 @@
 //     all 32 values of the next digit tested at once (radix passes over
 //     12-bit digits of (key - L) when there are more than 1024).
 //  4. Membership goes into two group bitmaps, key > s* and key == s*; one
-//     ballot / prefix-sum pass over the bitmap words then gives every member
-//     its slot in ascending position, the tie rule included.
+//     popcount / prefix-sum pass over the bitmap words then gives every
+//     member its place in ascending position, the tie rule included, and
+//     the member's own thread writes its four IDs there.
 // When the candidates do not fit in shared memory (e.g. when everything
 // ties) the CTA takes the plain path -- the same radix select and an ordered
 // emission over all G keys read from the scores.
@@ -457,8 +458,12 @@ select_emit_kernel(const SelectArgs a)
                 else if (key == thr) atomicOr(&sm.map_eq[g >> 5], 1u << (g & 31));
             }
             __syncthreads();
-            // ordered emission: thread t takes the words of groups 64t .. 64t+63
+            // Word prefixes: thread t takes the words of groups 64t .. 64t+63;
+            // #(key > s*) and #(key == s*) before each word go to shared
+            // memory (the radix histogram's space, free by now).
             constexpr int WPT = kMapWords / kThreads;  // 2
+            static_assert(2 * kMapWords <= kBins, "word prefixes fit in the histogram space");
+            uint32_t *pre_gt = sm.hist, *pre_eq = sm.hist + kMapWords;
             uint32_t wg[WPT], we[WPT], n_gt = 0, n_eq = 0;
 #pragma unroll
             for (int w = 0; w < WPT; ++w) {
@@ -473,31 +478,35 @@ select_emit_kernel(const SelectArgs a)
             uint32_t gt_c = uint32_t(before), eq_c = uint32_t(before >> 32);
 #pragma unroll
             for (int w = 0; w < WPT; ++w) {
-                uint32_t bits = wg[w] | we[w];
-                while (bits != 0u) {
-                    const int bpos = __ffs(bits) - 1;
-                    bits &= bits - 1u;
-                    const uint32_t bit = 1u << bpos;
-                    int pos = -1;
-                    if (wg[w] & bit) {
-                        pos = int(gt_c + min(need, eq_c));
-                        ++gt_c;
-                    } else {
-                        if (eq_c < need) pos = int(gt_c + eq_c);
-                        ++eq_c;
-                    }
-                    if (pos >= k) {  // cannot happen for a correct threshold; never write past the row
-                        set_error(a.err, QSA_DEVERR_ROW_RANGE);
-                        pos = -1;
-                    }
-                    if (pos >= 0) {
-                        const int g = 32 * (WPT * tid + w) + bpos;
-                        int32_t *o = row + kGroup * pos;
-                        o[0] = kGroup * g;
-                        o[1] = kGroup * g + 1;
-                        o[2] = kGroup * g + 2;
-                        o[3] = kGroup * g + 3;
-                    }
+                pre_gt[WPT * tid + w] = gt_c;
+                pre_eq[WPT * tid + w] = eq_c;
+                gt_c += __popc(wg[w]);
+                eq_c += __popc(we[w]);
+            }
+            __syncthreads();
+            // each member writes its IDs at #(key > s* before it) +
+            // min(need, #(key == s* before it)); equal keys past `need` are out
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t key = sm.cand_key[i];
+                if (key < thr) continue;
+                const int g = sm.cand_g[i];
+                const int wi = g >> 5;
+                const uint32_t below = (1u << (g & 31)) - 1u;
+                const uint32_t gt_b = pre_gt[wi] + __popc(sm.map_gt[wi] & below);
+                const uint32_t eq_b = pre_eq[wi] + __popc(sm.map_eq[wi] & below);
+                int pos = -1;
+                if (key > thr) pos = int(gt_b + min(need, eq_b));
+                else if (eq_b < need) pos = int(gt_b + eq_b);
+                if (pos >= k) {  // cannot happen for a correct threshold; never write past the row
+                    set_error(a.err, QSA_DEVERR_ROW_RANGE);
+                    pos = -1;
+                }
+                if (pos >= 0) {
+                    int32_t *o = row + kGroup * pos;
+                    o[0] = kGroup * g;
+                    o[1] = kGroup * g + 1;
+                    o[2] = kGroup * g + 2;
+                    o[3] = kGroup * g + 3;
                 }
             }
             done = true;
