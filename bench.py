@@ -339,6 +339,21 @@ def run_gpu(args):
 
     # ---- roofline of the dominant kernel (the scorer) --------------------------
     path_bytes, scorer_bytes = algorithmic_bytes(w)
+    # context for the scorer's fraction: a plain read-only stream of the same
+    # size on this GPU (torch.sum over a float32 buffer larger than L2)
+    rbuf = torch.ones(scorer_bytes // 4, dtype=torch.float32, device=db.out.device)
+    rsink = torch.zeros(1, dtype=torch.float32, device=db.out.device)
+    rev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    rms = []
+    for i in range(8):
+        rev[0].record(stream)
+        torch.sum(rbuf, dim=0, out=rsink[0])
+        rev[1].record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            rms.append(rev[0].elapsed_time(rev[1]))
+    read_gbs = rbuf.numel() * 4 / (float(np.median(rms)) * 1e-3) / 1e9
+    del rbuf
     peak, peak_src = measured_peaks()
     stage_mean = stage_ms.mean(axis=0)
     score_gbs = scorer_bytes / (stage_mean[0] * 1e-3) / 1e9
@@ -377,8 +392,11 @@ def run_gpu(args):
         "roofline": {"kernel": "score_groups", "bound": "hbm", "achieved": score_gbs,
                      "peak": peak, "unit": "GB/s", "frac": score_gbs / peak,
                      "traffic": profile_traffic(),
+                     "read_stream_gbs": read_gbs, "frac_of_read_stream": score_gbs / read_gbs,
                      "note": f"algorithmic bytes {scorer_bytes} per launch (raw index keys + "
-                             f"indexer queries + scores), peak = {peak_src} HBM copy bandwidth"},
+                             f"indexer queries + scores), peak = {peak_src} HBM copy bandwidth; "
+                             f"read_stream_gbs = torch.sum over a buffer of the same size, "
+                             f"same GPU, same run (a read-only stream, for context)"},
         "path_hbm": {"achieved_gbs": path_gbs, "frac_of_measured": path_gbs / peak,
                      "frac_of_8tbs": path_gbs / 8000.0, "algorithmic_bytes_per_step": path_bytes},
         "stages_us": {n: float(v * 1e3) for n, v in
