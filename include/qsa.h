@@ -197,8 +197,8 @@ qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t 
  * (KV head h / (n_q/n_kv)):
  *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
  * rows i < n_ids[b] visited in emitted order: the row is cut into runs of
- * 256 rows (9 at most), each run into groups of 32/r consecutive rows
- * (r = n_q/n_kv) dealt to 8 running states in turn; each state is a running
+ * 256 rows (9 at most), each run into steps of 8 consecutive rows dealt
+ * to 12 running states in turn; each state is a running
  * max / rescale / denominator / accumulator, and the states are merged in a
  * fixed order, then the runs in row order.  The split depends only on
  * n_ids[b], so results do not depend on the batch.  n_ids[b] = 0 gives a

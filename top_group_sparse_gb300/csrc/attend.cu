@@ -12,21 +12,21 @@
 // GPU order (fixed, documented, batch independent).  The emitted row of
 // query b is cut into runs of kRowsPerPart consecutive rows, one CTA per
 // (run, query b, KV head); the cut depends only on n_ids[b].  A run is cut
-// into steps of 8 consecutive rows, and step j goes to warp j mod 8, which
+// into steps of 8 consecutive rows, and step j goes to warp j mod 12, which
 // keeps its own online-softmax state for the GQ query heads of the KV head:
 // per step, scaled scores x_i, the new running max m' = max(m, max x_i), the
 // rescale e^(m - m') of the denominator l and of the accumulator, then
 // l += sum_i e^(x_i - m') and acc += sum_i e^(x_i - m') v_i.  At the end of
-// the run the eight warp states are merged in warp order (M = max m_w,
+// the run the twelve warp states are merged in warp order (M = max m_w,
 // L = sum l_w e^(m_w - M), acc = sum acc_w e^(m_w - M)), and the last CTA of
 // the (query, KV head) to finish -- an atomic ticket, nothing waits --
 // merges the runs in order the same way and divides by L.  No floating-point
 // atomics; the bits of a query's output do not depend on the rest of the batch.
 //
-// Data movement: the CTA's 256 threads resolve every row of its run at once
+// Data movement: the CTA's threads resolve every row of its run at once
 // (one row each: the ID load, then the slot-map load).  Each warp then
-// streams only its own steps through its own three-slot ring in shared
-// memory with 16-byte asynchronous copies, two steps ahead of its math, so no
+// streams only its own steps through its own two-slot ring in shared
+// memory with 16-byte asynchronous copies, one step ahead of its math, so no
 // thread-block barrier and no cross-warp wait sits inside the loop.
 //
 // Math of a step (8 rows x GQ heads).  Scores: lanes form HP = min(GQ, 4)
@@ -363,7 +363,7 @@ attend_kernel(const AttendArgs a)
     }
     cp_async_wait<0>();
 
-    // ---- this CTA's partial: the eight warp states merged in warp order ------------
+    // ---- this CTA's partial: the warp states merged in warp order --------------------
     __syncthreads();  // every warp is done with its ring: it becomes the reduction area
     float *red = &sm.k[0][0][0][0];  // [kWarps][GQ][D]
     if (col) {
