@@ -236,6 +236,49 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
                                int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream,
                                void *const *events, int32_t n_events);
 
+/* ---- the incremental form: a pooled-key cache --------------------------- */
+
+/* The notes pair the full-raw indexer with an incremental one ([AFN-017]
+ * capsule and Evidence: the full-raw / incremental identity): instead of
+ * pooling every group's raw keys at every decode step, keep the pooled key
+ * of each complete group in device memory and append groups as they
+ * complete.  The pooling arithmetic is the same binary32 sequence as in
+ * qsa_score_groups, so scores from the cache equal full-raw scores bit for
+ * bit, and so do the ID rows and outputs of qsa_decode_pooled.
+ *
+ * Cache layout (caller-owned, device): pooled[row][d_I] f32; group g of query
+ * b lives at row pool_offset[b] + g.  Queries that share a history may share
+ * rows (chunked prefill). */
+
+/* Appends pooled keys: for each query b and g in [group_begin[b],
+ * group_end[b]) (device int32 arrays),
+ *   pooled[pool_offset[b] + g][j] = (((k0[j]+k1[j])+k2[j])+k3[j]) * 0.25,
+ *   k_u = idx_keys[key_offset[b] + 4g + u]          (reads in->idx_keys,
+ * in->key_offset only).  max_groups (host) bounds group_end[b] -
+ * group_begin[b] for every b and sizes the launch: a decode step that
+ * completes one group per query passes 1.  The caller guarantees the raw rows
+ * exist.  A range outside [0, max_visible/4] or longer than max_groups is
+ * skipped and sets QSA_DEVERR_VISIBLE_RANGE. */
+qsa_status qsa_pool_groups(const qsa_dims *dims, const qsa_inputs *in, const int32_t *group_begin,
+                           const int32_t *group_end, int32_t max_groups, float *pooled,
+                           const int64_t *pool_offset, void *ws, size_t ws_bytes, void *stream);
+
+/* qsa_score_groups with the pooled keys read from the cache (rows
+ * pool_offset[b] + g, g < floor(T_b/4)) instead of pooled from the raw keys:
+ * G*d_I*4 bytes streamed per query instead of T*d_I*4.  Reads in->q_idx and
+ * in->visible; in->idx_keys and in->key_offset may be NULL. */
+qsa_status qsa_score_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
+                            const int64_t *pool_offset, float *scores, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/* qsa_decode with the scorer reading the pooled-key cache: same launches
+ * otherwise, same outputs bit for bit when the cache holds every complete
+ * group of each query's history.  in->idx_keys and in->key_offset may be
+ * NULL. */
+qsa_status qsa_decode_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
+                             const int64_t *pool_offset, int32_t *ids, int32_t *n_ids, float *out,
+                             void *ws, size_t ws_bytes, void *stream);
+
 /* ---- attention without a workspace -------------------------------------- */
 
 /* Fixed size of the device scratch behind qsa_attend_noalloc (4 MiB); every

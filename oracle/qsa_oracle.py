@@ -21,7 +21,7 @@ import numpy as np
 
 __all__ = [
     "build", "lib", "num_groups", "tail_len", "row_width", "pool_group",
-    "score_groups", "score_groups_incremental", "select", "dense_ids",
+    "score_groups", "score_groups_incremental", "pool_cache", "select", "dense_ids",
     "resolve", "attend", "decode", "GROUP",
 ]
 
@@ -168,12 +168,12 @@ def score_groups(q_idx: np.ndarray, keys: np.ndarray, T: int | None = None,
     return s[:G]
 
 
-def score_groups_incremental(q_idx: np.ndarray, keys: np.ndarray, T: int,
-                             pool_scale: float = 0.25) -> np.ndarray:
-    """Same scores, read from a pooled-key cache built one token at a time."""
-    q_idx, pq = _fa(q_idx)
+def pool_cache(keys: np.ndarray, T: int, pool_scale: float = 0.25) -> np.ndarray:
+    """The pooled-key cache of one history after T tokens, built one token at
+    a time as a decode loop would ("full-raw / incremental identity"):
+    [floor(T/4), d] pooled keys of the complete groups."""
     keys = np.ascontiguousarray(keys, dtype=np.float32)
-    H, d = q_idx.shape
+    d = keys.shape[1]
     G = T // GROUP
     pooled = np.zeros((max(G, 1), d), np.float32)
     pending = np.zeros((GROUP, d), np.float32)
@@ -182,8 +182,20 @@ def score_groups_incremental(q_idx: np.ndarray, keys: np.ndarray, T: int,
     for t in range(T):
         row = keys[t]
         L.qsao_pool_cache_append(pp, pe, d, row.ctypes.data_as(_F32P), t, pool_scale)
+    return pooled[:G]
+
+
+def score_groups_incremental(q_idx: np.ndarray, keys: np.ndarray, T: int,
+                             pool_scale: float = 0.25) -> np.ndarray:
+    """Same scores, read from a pooled-key cache built one token at a time."""
+    q_idx, pq = _fa(q_idx)
+    H, d = q_idx.shape
+    G = T // GROUP
+    pooled = np.ascontiguousarray(pool_cache(keys, T, pool_scale))
+    if G == 0:
+        pooled = np.zeros((1, d), np.float32)
     s = np.empty(max(G, 1), np.float32)
-    L.qsao_score_from_pooled(pq, H, d, pp, G, s.ctypes.data_as(_F32P))
+    lib().qsao_score_from_pooled(pq, H, d, pooled.ctypes.data_as(_F32P), G, s.ctypes.data_as(_F32P))
     return s[:G]
 
 

@@ -91,6 +91,15 @@ qsa_status check_inputs_score(const qsa_inputs *in)
     return QSA_OK;
 }
 
+// Scoring from the pooled-key cache reads q_idx and visible from `in`.
+qsa_status check_inputs_pooled(const qsa_inputs *in, const float *pooled, const int64_t *pool_offset)
+{
+    if (!in || !in->q_idx || !in->visible || !pooled || !pool_offset) return QSA_ERR_INVALID_ARG;
+    if (!aligned(in->q_idx, 16) || !aligned(in->visible, 4) || !aligned(pooled, 16) || !aligned(pool_offset, 8))
+        return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
 qsa_status check_inputs_gather(const qsa_inputs *in)
 {
     if (!in || !in->visible || !in->k_cache || !in->v_cache || !in->slot_map || !in->slot_offset)
@@ -115,15 +124,17 @@ T *ws_at(void *ws, size_t off)
     return reinterpret_cast<T *>(static_cast<unsigned char *>(ws) + off);
 }
 
+// pooled != nullptr: score from the pooled-key cache instead of the raw keys.
 qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int64_t stride, void *ws,
-                    const Layout &L, cudaStream_t s)
+                    const Layout &L, cudaStream_t s, const float *pooled = nullptr,
+                    const int64_t *pool_offset = nullptr)
 {
     if (d->batch == 0) return QSA_OK;
     const int sms = num_sms_of_current_device();
     if (sms <= 0) return QSA_ERR_CUDA;
     ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, stride,
                 d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L),
-                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride};
+                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride, pooled, pool_offset};
     return from_cuda(launch_score(a, sms, s));
 }
 
@@ -340,14 +351,18 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
     return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, static_cast<cudaStream_t>(stream));
 }
 
-qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids,
-                               float *out, void *ws, size_t ws_bytes, void *stream, void *const *events,
-                               int32_t n_events)
+}  // extern "C"
+
+namespace {
+// The whole path; pooled != nullptr scores from the pooled-key cache.
+qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
+                       const int64_t *pool_offset, int32_t *ids, int32_t *n_ids, float *out, void *ws,
+                       size_t ws_bytes, void *stream, void *const *events, int32_t n_events)
 {
     if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
     qsa_status st;
     if ((st = check_shapes(dims, true, true)) != QSA_OK) return st;
-    if ((st = check_inputs_score(in)) != QSA_OK) return st;
+    if ((st = pooled ? check_inputs_pooled(in, pooled, pool_offset) : check_inputs_score(in)) != QSA_OK) return st;
     if ((st = check_inputs_gather(in)) != QSA_OK) return st;
     if (!in->q || !aligned(in->q, 16)) return QSA_ERR_INVALID_ARG;
     if (!ids || !n_ids || !out || !aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(out, 16))
@@ -363,7 +378,7 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
         return n_events == 0 || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     };
     if (!mark(0)) return QSA_ERR_CUDA;
-    if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s)) != QSA_OK) return st;
+    if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s, pooled, pool_offset)) != QSA_OK) return st;
     if (!mark(1)) return QSA_ERR_CUDA;
     // The three launches overlap their launch latency with the predecessor's
     // tail (programmatic dependent launch) unless timing marks separate them.
@@ -375,6 +390,59 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
     if ((st = do_gather_attend(dims, in, ids, n_ids, nullptr, nullptr, out, ws, L, s, pdl)) != QSA_OK) return st;
     if (!mark(3)) return QSA_ERR_CUDA;
     return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids,
+                               float *out, void *ws, size_t ws_bytes, void *stream, void *const *events,
+                               int32_t n_events)
+{
+    return decode_impl(dims, in, nullptr, nullptr, ids, n_ids, out, ws, ws_bytes, stream, events, n_events);
+}
+
+qsa_status qsa_decode_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
+                             const int64_t *pool_offset, int32_t *ids, int32_t *n_ids, float *out, void *ws,
+                             size_t ws_bytes, void *stream)
+{
+    if (!pooled || !pool_offset) return QSA_ERR_INVALID_ARG;
+    return decode_impl(dims, in, pooled, pool_offset, ids, n_ids, out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+qsa_status qsa_score_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
+                            const int64_t *pool_offset, float *scores, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, true, false)) != QSA_OK) return st;
+    if ((st = check_inputs_pooled(in, pooled, pool_offset)) != QSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_score(dims, in, scores, L.score_stride, ws, L, static_cast<cudaStream_t>(stream), pooled, pool_offset);
+}
+
+qsa_status qsa_pool_groups(const qsa_dims *dims, const qsa_inputs *in, const int32_t *group_begin,
+                           const int32_t *group_end, int32_t max_groups, float *pooled, const int64_t *pool_offset,
+                           void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    if (!score_shape_supported(dims->idx_heads, dims->idx_dim)) return QSA_ERR_UNSUPPORTED_SHAPE;
+    if (!in || !in->idx_keys || !in->key_offset || !aligned(in->idx_keys, 16) || !aligned(in->key_offset, 8))
+        return QSA_ERR_INVALID_ARG;
+    if (!group_begin || !group_end || !pooled || !pool_offset || !aligned(group_begin, 4) ||
+        !aligned(group_end, 4) || !aligned(pooled, 16) || !aligned(pool_offset, 8))
+        return QSA_ERR_INVALID_ARG;
+    const int32_t g_max = dims->max_visible / kGroup;
+    if (max_groups < 0 || max_groups > g_max) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    PoolArgs a{in->idx_keys, in->key_offset, group_begin, group_end, pooled, pool_offset,
+               dims->batch, dims->idx_dim, max_groups, g_max, err_word(ws, L)};
+    return from_cuda(launch_pool(a, static_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids, float *out,

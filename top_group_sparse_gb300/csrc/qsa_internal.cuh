@@ -70,9 +70,24 @@ struct ScoreArgs {
     uint32_t *err;
     uint32_t *qmax;          // [B, qmax_stride]: order key of the max score of groups 4j..4j+3
     int64_t qmax_stride;
+    // pooled != nullptr: score from the pooled-key cache, group g of query b
+    // at row pool_offset[b] + g (idx_keys, key_offset unused)
+    const float *pooled;
+    const int64_t *pool_offset;
 };
 bool score_shape_supported(int idx_heads, int idx_dim);
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
+
+struct PoolArgs {
+    const float *idx_keys;
+    const int64_t *key_offset;
+    const int32_t *group_begin, *group_end;
+    float *pooled;
+    const int64_t *pool_offset;
+    int32_t batch, idx_dim, max_groups, g_max;
+    uint32_t *err;
+};
+cudaError_t launch_pool(const PoolArgs &a, cudaStream_t s);
 
 // pdl: launch programmatically after the previous kernel in the stream
 // (used only inside qsa_decode, where the order of the launches is fixed).

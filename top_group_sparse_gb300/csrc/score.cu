@@ -25,16 +25,35 @@
 // double-buffered pooled tile (one barrier per tile); then thread (g, h) runs
 // the D-long FMA chain of head h for group g with q_h in registers, and the H
 // head results are summed in order after a warp shuffle gather.
+//
+// The same kernel scores from a pooled-key cache (the incremental form: the
+// pooled key of every complete group kept in device memory, appended as
+// groups complete): then a stage holds pooled rows, the pooling step becomes
+// a copy into the swizzled tile, and the stream is G * D * 4 bytes per query
+// instead of T * D * 4.  pool_groups_kernel fills that cache with the very
+// pooling arithmetic of the raw path (pool4 below), so both forms give the
+// same scores bit for bit -- the full-raw / incremental identity.
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-template <int H, int D>
+// p = (((k0 + k1) + k2) + k3) * 0.25 in binary32, round to nearest, per lane.
+__device__ __forceinline__ float4 pool4(float4 k0, float4 k1, float4 k2, float4 k3)
+{
+    float4 p;
+    p.x = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.x, k1.x), k2.x), k3.x), 0.25f);
+    p.y = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.y, k1.y), k2.y), k3.y), 0.25f);
+    p.z = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.z, k1.z), k2.z), k3.z), 0.25f);
+    p.w = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.w, k1.w), k2.w), k3.w), 0.25f);
+    return p;
+}
+
+template <int H, int D, bool kPooled>
 struct ScoreCfg {
     static constexpr int kThreads = 256;
     static constexpr int kTG = kThreads / H;                // groups per tile
-    static constexpr int kGroupFloats = kGroup * D;         // raw floats per group
+    static constexpr int kGroupFloats = kPooled ? D : kGroup * D;  // stage floats per group
     static constexpr int kStageFloats = kTG * kGroupFloats;
     static constexpr int kStageBytes = kStageFloats * 4;
     // Two CTAs per SM when a stage is small enough, so that one CTA's
@@ -101,11 +120,11 @@ __device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int end, int
     return end;
 }
 
-template <int H, int D>
-__global__ void __launch_bounds__(ScoreCfg<H, D>::kThreads, ScoreCfg<H, D>::kCtasPerSm)
+template <int H, int D, bool kPooled>
+__global__ void __launch_bounds__(ScoreCfg<H, D, kPooled>::kThreads, ScoreCfg<H, D, kPooled>::kCtasPerSm)
 score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 {
-    using C = ScoreCfg<H, D>;
+    using C = ScoreCfg<H, D, kPooled>;
     constexpr int F4 = D / 4;
     extern __shared__ __align__(128) unsigned char smem[];
     float *stages = reinterpret_cast<float *>(smem);
@@ -147,10 +166,11 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         t_issue = next_tile<C::kTG>(a, t_issue, t_end, tiles_per_q, qc_issue, r);
         if (t_issue >= t_end) return;
         if (r.b != koff_b) {
-            koff = __ldg(a.key_offset + r.b);
+            koff = __ldg((kPooled ? a.pool_offset : a.key_offset) + r.b);
             koff_b = r.b;
         }
-        const float *src = a.idx_keys + (koff + int64_t(r.g0) * kGroup) * D;
+        const float *src = kPooled ? a.pooled + (koff + int64_t(r.g0)) * D
+                                   : a.idx_keys + (koff + int64_t(r.g0) * kGroup) * D;
         const uint32_t bytes = uint32_t(r.n) * C::kGroupFloats * 4u;
         mbar_arrive_expect_tx(&full[stage], bytes);
         bulk_copy_g2s_hint(stages + size_t(stage) * C::kStageFloats, src, bytes, &full[stage], policy);
@@ -190,18 +210,19 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
 
-        // Pool, 16 bytes per item: item e is (group e / F4, chunk e % F4).
+        // Pool (or, from the pooled cache, copy), 16 bytes per item: item e is
+        // (group e / F4, chunk e % F4).
         const float4 *raw = reinterpret_cast<const float4 *>(stages + size_t(s) * C::kStageFloats);
         for (int e = tid; e < r.n * F4; e += C::kThreads) {
             const int g = e / F4;
             const int j4 = e - g * F4;
-            const float4 *k = raw + g * (kGroup * F4) + j4;
-            const float4 k0 = k[0], k1 = k[F4], k2 = k[2 * F4], k3 = k[3 * F4];
             float4 p;
-            p.x = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.x, k1.x), k2.x), k3.x), 0.25f);
-            p.y = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.y, k1.y), k2.y), k3.y), 0.25f);
-            p.z = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.z, k1.z), k2.z), k3.z), 0.25f);
-            p.w = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.w, k1.w), k2.w), k3.w), 0.25f);
+            if constexpr (kPooled) {
+                p = raw[g * F4 + j4];
+            } else {
+                const float4 *k = raw + g * (kGroup * F4) + j4;
+                p = pool4(k[0], k[F4], k[2 * F4], k[3 * F4]);
+            }
             *reinterpret_cast<float4 *>(pool + pool_index<D>(g, j4)) = p;
         }
         // One barrier per tile: the pooled tile is ready and raw stage s is
@@ -255,10 +276,10 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     }
 }
 
-template <int H, int D>
+template <int H, int D, bool kPooled>
 cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
 {
-    using C = ScoreCfg<H, D>;
+    using C = ScoreCfg<H, D, kPooled>;
     const int gmax = a.max_visible / kGroup;
     const int tiles_per_q = (gmax + C::kTG - 1) / C::kTG;
     const long long total = (long long)a.batch * tiles_per_q;
@@ -269,18 +290,50 @@ cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (resident[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(score_groups_kernel<H, D>,
+        cudaError_t e = cudaFuncSetAttribute(score_groups_kernel<H, D, kPooled>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_groups_kernel<H, D>, C::kThreads, C::kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_groups_kernel<H, D, kPooled>, C::kThreads, C::kSmem);
         if (e != cudaSuccess) return e;
         resident[dev] = per_sm > 0 ? per_sm : 1;
     }
     const long long slots = (long long)num_sms * resident[dev];
     const int grid = int(total < slots ? total : slots);
-    score_groups_kernel<H, D><<<grid, C::kThreads, C::kSmem, s>>>(a, tiles_per_q);
+    score_groups_kernel<H, D, kPooled><<<grid, C::kThreads, C::kSmem, s>>>(a, tiles_per_q);
     return cudaGetLastError();
+}
+
+
+// ---- the pooled-key cache ------------------------------------------------------
+
+constexpr int kPoolThreads = 256;
+constexpr int kPoolGroupsPerCta = 64;
+
+// pooled[pool_offset[b] + g] = pool of raw rows key_offset[b] + 4g .. 4g+3,
+// for g in [group_begin[b], group_end[b]).  One 16-byte chunk per thread-item.
+template <int D>
+__global__ void __launch_bounds__(kPoolThreads)
+pool_groups_kernel(const PoolArgs a)
+{
+    constexpr int F4 = D / 4;
+    const int b = blockIdx.y;
+    const int g_begin = __ldg(a.group_begin + b), g_end = __ldg(a.group_end + b);
+    if (g_begin < 0 || g_end < g_begin || g_end > a.g_max || g_end - g_begin > a.max_groups) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, QSA_DEVERR_VISIBLE_RANGE);
+        return;
+    }
+    const int g_lo = g_begin + int(blockIdx.x) * kPoolGroupsPerCta;
+    const int g_hi = min(g_end, g_lo + kPoolGroupsPerCta);
+    if (g_lo >= g_hi) return;
+    const float4 *keys = reinterpret_cast<const float4 *>(a.idx_keys + __ldg(a.key_offset + b) * D);
+    float4 *out = reinterpret_cast<float4 *>(a.pooled + __ldg(a.pool_offset + b) * D);
+    for (int e = threadIdx.x; e < (g_hi - g_lo) * F4; e += kPoolThreads) {
+        const int g = g_lo + e / F4;
+        const int j4 = e % F4;
+        const float4 *k = keys + int64_t(g) * (kGroup * F4) + j4;
+        out[int64_t(g) * F4 + j4] = pool4(__ldg(k), __ldg(k + F4), __ldg(k + 2 * F4), __ldg(k + 3 * F4));
+    }
 }
 
 }  // namespace
@@ -292,11 +345,26 @@ bool score_shape_supported(int idx_heads, int idx_dim)
 
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s)
 {
-    if (a.idx_heads == 8 && a.idx_dim == 64) return launch_score_t<8, 64>(a, num_sms, s);
-    if (a.idx_heads == 4 && a.idx_dim == 32) return launch_score_t<4, 32>(a, num_sms, s);
-    if (a.idx_heads == 8 && a.idx_dim == 32) return launch_score_t<8, 32>(a, num_sms, s);
-    if (a.idx_heads == 4 && a.idx_dim == 64) return launch_score_t<4, 64>(a, num_sms, s);
+    const bool pooled = a.pooled != nullptr;
+    if (a.idx_heads == 8 && a.idx_dim == 64)
+        return pooled ? launch_score_t<8, 64, true>(a, num_sms, s) : launch_score_t<8, 64, false>(a, num_sms, s);
+    if (a.idx_heads == 4 && a.idx_dim == 32)
+        return pooled ? launch_score_t<4, 32, true>(a, num_sms, s) : launch_score_t<4, 32, false>(a, num_sms, s);
+    if (a.idx_heads == 8 && a.idx_dim == 32)
+        return pooled ? launch_score_t<8, 32, true>(a, num_sms, s) : launch_score_t<8, 32, false>(a, num_sms, s);
+    if (a.idx_heads == 4 && a.idx_dim == 64)
+        return pooled ? launch_score_t<4, 64, true>(a, num_sms, s) : launch_score_t<4, 64, false>(a, num_sms, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pool(const PoolArgs &a, cudaStream_t s)
+{
+    if (a.batch == 0 || a.max_groups == 0) return cudaSuccess;
+    const dim3 grid(unsigned((a.max_groups + kPoolGroupsPerCta - 1) / kPoolGroupsPerCta), unsigned(a.batch));
+    if (a.idx_dim == 64) pool_groups_kernel<64><<<grid, kPoolThreads, 0, s>>>(a);
+    else if (a.idx_dim == 32) pool_groups_kernel<32><<<grid, kPoolThreads, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 }  // namespace qsa

@@ -18,7 +18,8 @@ __all__ = [
     "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
     "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode",
-    "qsa_decode_profiled", "qsa_attend_noalloc",
+    "qsa_decode_profiled", "qsa_attend_noalloc", "qsa_pool_groups", "qsa_score_pooled",
+    "qsa_decode_pooled",
     "make_dims",
     "DeviceBatch",
     "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
@@ -117,6 +118,12 @@ def load(path: str | None = None):
     L.qsa_decode_profiled.restype = ctypes.c_int
     L.qsa_attend_noalloc.argtypes = [_DP, _P, _P, _P, _P, _P, _P]
     L.qsa_attend_noalloc.restype = ctypes.c_int
+    L.qsa_pool_groups.argtypes = [_DP, _IP, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_pool_groups.restype = ctypes.c_int
+    L.qsa_score_pooled.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_score_pooled.restype = ctypes.c_int
+    L.qsa_decode_pooled.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_decode_pooled.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -270,6 +277,28 @@ def qsa_decode_profiled(dims, inputs, ids, n_ids, out, ws, events, stream=None) 
         _stream(stream), arr, len(handles)))
 
 
+def qsa_pool_groups(dims, inputs, group_begin, group_end, max_groups, pooled, pool_offset, ws,
+                    stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_pool_groups", load().qsa_pool_groups(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(group_begin), _ptr(group_end), int(max_groups),
+        _ptr(pooled), _ptr(pool_offset), p, n, _stream(stream)))
+
+
+def qsa_score_pooled(dims, inputs, pooled, pool_offset, scores, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_score_pooled", load().qsa_score_pooled(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(pooled), _ptr(pool_offset), _ptr(scores), p, n,
+        _stream(stream)))
+
+
+def qsa_decode_pooled(dims, inputs, pooled, pool_offset, ids, n_ids, out, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_decode_pooled", load().qsa_decode_pooled(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(pooled), _ptr(pool_offset), _ptr(ids),
+        _ptr(n_ids), _ptr(out), p, n, _stream(stream)))
+
+
 def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
     """Attention stage with the library's fixed static scratch instead of a
     workspace, for callers that cannot allocate device memory."""
@@ -351,6 +380,53 @@ class DeviceBatch:
     def decode_profiled(self, events, stream=None):
         return qsa_decode_profiled(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws,
                                    events, stream)
+
+    # ---- the incremental form: a pooled-key cache -----------------------------
+    def make_pooled_cache(self):
+        """Allocates the pooled-key cache: one block of rows per distinct
+        history (queries that share a history share its rows), room for the
+        longest T over the queries of that history."""
+        import torch
+        ko = self.key_offset.cpu().numpy()
+        T = self.visible.cpu().numpy()
+        base, rows = {}, 0
+        for k in sorted(set(ko.tolist())):
+            base[k] = rows
+            rows += int(T[ko == k].max()) // 4
+        self.pool_offset = torch.from_numpy(np.array([base[k] for k in ko.tolist()], np.int64)).to(self.q.device)
+        self.pooled = torch.zeros((max(rows, 1), self.w.idx_dim), dtype=torch.float32, device=self.q.device)
+        # the query of each history with the longest T pools the history's groups
+        owner = {}
+        for b, k in enumerate(ko.tolist()):
+            if k not in owner or T[b] > T[owner[k]]:
+                owner[k] = b
+        self._pool_owner = np.array([owner[k] == b for b, k in enumerate(ko.tolist())])
+        return self.pooled
+
+    def pool(self, group_begin, group_end, stream=None):
+        """Appends groups [group_begin[b], group_end[b]) of every query (host arrays)."""
+        import torch
+        gb = np.asarray(group_begin, np.int32)
+        ge = np.asarray(group_end, np.int32)
+        mg = int((ge - gb).max(initial=0))
+        dev = self.q.device
+        self._pool_args = (torch.from_numpy(gb).to(dev), torch.from_numpy(ge).to(dev))
+        return qsa_pool_groups(self.dims, self.inputs, self._pool_args[0], self._pool_args[1], max(mg, 0),
+                               self.pooled, self.pool_offset, self.ws, stream)
+
+    def pool_all(self, stream=None):
+        """Pools every complete group of every history (once per history)."""
+        G = (self.visible.cpu().numpy() // 4).astype(np.int32)
+        ge = np.where(self._pool_owner, G, 0).astype(np.int32)
+        return self.pool(np.zeros_like(ge), ge, stream)
+
+    def score_pooled(self, stream=None):
+        return qsa_score_pooled(self.dims, self.inputs, self.pooled, self.pool_offset, self.scores,
+                                self.ws, stream)
+
+    def decode_pooled(self, stream=None):
+        return qsa_decode_pooled(self.dims, self.inputs, self.pooled, self.pool_offset, self.ids,
+                                 self.n_ids, self.out, self.ws, stream)
 
     def check_errors(self, stream=None):
         return qsa_check_errors(self.ws, stream)
