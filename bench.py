@@ -338,6 +338,44 @@ def run_gpu(args):
     inc_value = ws * w.batch * K4 / (inc_ms / 1e3)
     del db.pooled
 
+    # ---- chunked prefill: 256 queries over one history, per-query vs shared ----
+    chunk = None
+    if not args.no_chunked:
+        wc = wl.chunked_prefill_100000()
+        dc = qsa.DeviceBatch(wc, device=f"cuda:{local}")
+
+        def time_path(fn, n=50):
+            for _ in range(3):
+                flush()
+                fn(stream)
+            torch.cuda.synchronize()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            for ev in evs:
+                for e in ev:
+                    e.record(stream)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(20_000_000)
+            for ev in evs:
+                flush()
+                ev[0].record(stream)
+                fn(stream)
+                ev[1].record(stream)
+            torch.cuda.synchronize()
+            return float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+
+        ms_shared = time_path(dc.decode_shared)
+        ms_single = time_path(dc.decode)
+        st, flags = dc.check_errors()
+        if st != 0:
+            raise SystemExit(f"device error word {flags:#x} in the chunked-prefill loop")
+        chunk = {"workload": "chunked_prefill_100000", "queries_per_step": wc.batch,
+                 "shared": {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared},
+                 "per_query": {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single},
+                 "note": "256 queries at positions 100,000..100,255 of one history: qsa_decode_shared "
+                         "(each pooled tile scored for every query) vs qsa_decode (each query streams "
+                         "its own keys); outputs bit-identical (tests); L2 flushed before each step"}
+        del dc
+
     # ---- end to end through qsa_decode with host buffers -----------------------
     K2 = max(1, min(K, args.e2e_steps))
     h_qidx = torch.from_numpy(w.q_idx).pin_memory()
@@ -429,6 +467,7 @@ def run_gpu(args):
                                 "(G*d_I*4 bytes per query instead of T*d_I*4): one qsa_pool_groups "
                                 "append of one group per query + qsa_decode_pooled per step; rows and "
                                 "outputs bit-identical to the full-raw path (tests)"},
+        "chunked_prefill": chunk,
         "stages_us": {n: float(v * 1e3) for n, v in
                       zip(("score", "select", "gather_attend"), stage_mean)},
         "loop_wall_s": loop_wall,
@@ -453,6 +492,7 @@ def main():
                     help="queries per GPU (8 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill side measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -62,6 +62,8 @@ typedef enum {
 #define QSA_DEVERR_SLOT_RANGE    0x2u  /* a slot-map entry outside the cache  */
 #define QSA_DEVERR_ROW_RANGE     0x4u  /* n_ids[b] or an ID outside its row   */
 #define QSA_DEVERR_WAIT_TIMEOUT  0x8u  /* a bounded copy wait ran out         */
+#define QSA_DEVERR_NOT_SHARED    0x10u /* a shared-history call whose queries  */
+                                       /* do not all have key_offset[0]       */
 
 /* Problem dimensions.  Supported builds: (idx_heads, idx_dim) in
  * {(4,32), (8,32), (4,64), (8,64)}; head_dim in {64, 128};
@@ -278,6 +280,24 @@ qsa_status qsa_score_pooled(const qsa_dims *dims, const qsa_inputs *in, const fl
 qsa_status qsa_decode_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
                              const int64_t *pool_offset, int32_t *ids, int32_t *n_ids, float *out,
                              void *ws, size_t ws_bytes, void *stream);
+
+/* ---- queries over one shared history (chunked prefill) ------------------ */
+
+/* qsa_score_groups for a batch whose queries all read one key history
+ * (key_offset[b] == key_offset[0] for every b; T_b may differ), e.g. the
+ * consecutive positions of a chunked prefill ([AFN-017] capsule: chunk =
+ * decode).  Each tile of raw keys is pooled once and scored for every query
+ * that needs it, instead of once per query; the scores are bit-identical to
+ * qsa_score_groups.  A query whose key_offset differs gets no scores and
+ * sets QSA_DEVERR_NOT_SHARED. */
+qsa_status qsa_score_groups_shared(const qsa_dims *dims, const qsa_inputs *in, float *scores,
+                                   void *ws, size_t ws_bytes, void *stream);
+
+/* qsa_decode with the shared-history scorer: same launches otherwise, and
+ * outputs bit-identical to qsa_decode (and so to one single-query decode per
+ * query). */
+qsa_status qsa_decode_shared(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
+                             int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 
 /* ---- attention without a workspace -------------------------------------- */
 

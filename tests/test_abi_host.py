@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 18
+    assert len(names) == 20
     for n in names:
         assert hasattr(lib, n), n
     for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",

@@ -124,10 +124,11 @@ T *ws_at(void *ws, size_t off)
     return reinterpret_cast<T *>(static_cast<unsigned char *>(ws) + off);
 }
 
-// pooled != nullptr: score from the pooled-key cache instead of the raw keys.
+// pooled != nullptr: score from the pooled-key cache instead of the raw keys;
+// shared: every query reads the history at key_offset[0] (one pooled tile for all).
 qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int64_t stride, void *ws,
                     const Layout &L, cudaStream_t s, const float *pooled = nullptr,
-                    const int64_t *pool_offset = nullptr)
+                    const int64_t *pool_offset = nullptr, bool shared = false)
 {
     if (d->batch == 0) return QSA_OK;
     const int sms = num_sms_of_current_device();
@@ -135,7 +136,7 @@ qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int6
     ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, stride,
                 d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L),
                 ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride, pooled, pool_offset};
-    return from_cuda(launch_score(a, sms, s));
+    return from_cuda(shared ? launch_score_shared(a, sms, s) : launch_score(a, sms, s));
 }
 
 // use_hint: the quad maxima in the workspace were written by the scorer for
@@ -357,7 +358,8 @@ namespace {
 // The whole path; pooled != nullptr scores from the pooled-key cache.
 qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
                        const int64_t *pool_offset, int32_t *ids, int32_t *n_ids, float *out, void *ws,
-                       size_t ws_bytes, void *stream, void *const *events, int32_t n_events)
+                       size_t ws_bytes, void *stream, void *const *events, int32_t n_events,
+                       bool shared = false)
 {
     if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
     qsa_status st;
@@ -378,7 +380,8 @@ qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *
         return n_events == 0 || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
     };
     if (!mark(0)) return QSA_ERR_CUDA;
-    if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s, pooled, pool_offset)) != QSA_OK) return st;
+    if ((st = do_score(dims, in, scores, L.score_stride, ws, L, s, pooled, pool_offset, shared)) != QSA_OK)
+        return st;
     if (!mark(1)) return QSA_ERR_CUDA;
     // The three launches overlap their launch latency with the predecessor's
     // tail (programmatic dependent launch) unless timing marks separate them.
@@ -409,6 +412,26 @@ qsa_status qsa_decode_pooled(const qsa_dims *dims, const qsa_inputs *in, const f
 {
     if (!pooled || !pool_offset) return QSA_ERR_INVALID_ARG;
     return decode_impl(dims, in, pooled, pool_offset, ids, n_ids, out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+qsa_status qsa_decode_shared(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids, int32_t *n_ids,
+                             float *out, void *ws, size_t ws_bytes, void *stream)
+{
+    return decode_impl(dims, in, nullptr, nullptr, ids, n_ids, out, ws, ws_bytes, stream, nullptr, 0, true);
+}
+
+qsa_status qsa_score_groups_shared(const qsa_dims *dims, const qsa_inputs *in, float *scores, void *ws,
+                                   size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, true, false)) != QSA_OK) return st;
+    if ((st = check_inputs_score(in)) != QSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_score(dims, in, scores, L.score_stride, ws, L, static_cast<cudaStream_t>(stream), nullptr, nullptr,
+                    true);
 }
 
 qsa_status qsa_score_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,

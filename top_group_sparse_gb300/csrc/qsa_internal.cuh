@@ -77,6 +77,8 @@ struct ScoreArgs {
 };
 bool score_shape_supported(int idx_heads, int idx_dim);
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
+// every query of the batch reads the history at key_offset[0] (checked on the device)
+cudaError_t launch_score_shared(const ScoreArgs &a, int num_sms, cudaStream_t s);
 
 struct PoolArgs {
     const float *idx_keys;

@@ -33,26 +33,20 @@
 // instead of T * D * 4.  pool_groups_kernel fills that cache with the very
 // pooling arithmetic of the raw path (pool4 below), so both forms give the
 // same scores bit for bit -- the full-raw / incremental identity.
+#include "pooling.cuh"
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-// p = (((k0 + k1) + k2) + k3) * 0.25 in binary32, round to nearest, per lane.
-__device__ __forceinline__ float4 pool4(float4 k0, float4 k1, float4 k2, float4 k3)
-{
-    float4 p;
-    p.x = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.x, k1.x), k2.x), k3.x), 0.25f);
-    p.y = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.y, k1.y), k2.y), k3.y), 0.25f);
-    p.z = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.z, k1.z), k2.z), k3.z), 0.25f);
-    p.w = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(k0.w, k1.w), k2.w), k3.w), 0.25f);
-    return p;
-}
-
 template <int H, int D, bool kPooled>
 struct ScoreCfg {
     static constexpr int kThreads = 256;
-    static constexpr int kTG = kThreads / H;                // groups per tile
+    // groups per thread per tile: the pooled form moves 4x fewer bytes per
+    // group, so each thread runs four independent FMA chains per tile
+    static constexpr int kGPT = kPooled ? 4 : 1;
+    static constexpr int kTG1 = kThreads / H;               // groups per pass of the CTA
+    static constexpr int kTG = kTG1 * kGPT;                 // groups per tile
     static constexpr int kGroupFloats = kPooled ? D : kGroup * D;  // stage floats per group
     static constexpr int kStageFloats = kTG * kGroupFloats;
     static constexpr int kStageBytes = kStageFloats * 4;
@@ -63,7 +57,9 @@ struct ScoreCfg {
     static constexpr int kStageBudget = kCtasPerSm == 2 ? 98304 : 196608;
     static constexpr int kStagesRaw = kStageBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-    static constexpr int kPoolFloats = kTG * D;             // one pooled tile (swizzled)
+    // one pooled tile (swizzled), double buffered; the pooled form reads its
+    // stage directly and needs none
+    static constexpr int kPoolFloats = kPooled ? 0 : kTG * D;
     static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * size_t(kPoolFloats) * 4 + kStages * 8;
     static_assert(kThreads % H == 0 && 32 % (4 * H) == 0, "a warp holds whole quads of groups");
     static_assert(kTG % 4 == 0, "tiles start on quad boundaries");
@@ -71,13 +67,6 @@ struct ScoreCfg {
     static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
-// Pooled tile layout: group g's 16-byte chunk j4 sits at chunk (j4 ^ (g & 7))
-// of row g, so the 4 or 8 groups a warp reads at once hit distinct banks.
-template <int D>
-__device__ __forceinline__ int pool_index(int g, int j4)
-{
-    return g * D + ((j4 ^ (g & 7)) << 2);
-}
 
 // Per-query values a thread needs, reloaded only when the query changes.
 struct QueryCache {
@@ -210,59 +199,76 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
         const bool ok = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
 
-        // Pool (or, from the pooled cache, copy), 16 bytes per item: item e is
-        // (group e / F4, chunk e % F4).
-        const float4 *raw = reinterpret_cast<const float4 *>(stages + size_t(s) * C::kStageFloats);
-        for (int e = tid; e < r.n * F4; e += C::kThreads) {
-            const int g = e / F4;
-            const int j4 = e - g * F4;
-            float4 p;
-            if constexpr (kPooled) {
-                p = raw[g * F4 + j4];
-            } else {
+        if constexpr (!kPooled) {
+            // Pool, 16 bytes per item: item e is (group e / F4, chunk e % F4).
+            const float4 *raw = reinterpret_cast<const float4 *>(stages + size_t(s) * C::kStageFloats);
+            for (int e = tid; e < r.n * F4; e += C::kThreads) {
+                const int g = e / F4;
+                const int j4 = e - g * F4;
                 const float4 *k = raw + g * (kGroup * F4) + j4;
-                p = pool4(k[0], k[F4], k[2 * F4], k[3 * F4]);
+                *reinterpret_cast<float4 *>(pool + pool_index<D>(g, j4)) = pool4(k[0], k[F4], k[2 * F4], k[3 * F4]);
             }
-            *reinterpret_cast<float4 *>(pool + pool_index<D>(g, j4)) = p;
+            // One barrier per tile: the pooled tile is ready and raw stage s is
+            // consumed.  (The pooled tile is double buffered, so the next tile's
+            // pooling cannot overwrite what slower threads still read.)
+            if (__syncthreads_or(!ok)) {
+                timed_out = true;
+                break;
+            }
+            if (tid == 0) issue(s);  // refill stage s with the tile kStages ahead
         }
-        // One barrier per tile: the pooled tile is ready and raw stage s is
-        // consumed.  (The pooled tile is double buffered, so the next tile's
-        // pooling cannot overwrite what slower threads still read.)
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        if (tid == 0) issue(s);  // refill stage s with the tile kStages ahead
+        // (the pooled form reads its stage in place: one barrier per tile,
+        // after the dots, settles a timed-out wait and frees the stage)
 
-        float relu = 0.0f;
-        if (gl < r.n) {
-            float acc = 0.0f;
+        // Dots: groups gl + kTG1 * i of the tile, i < kGPT, each a D-long chain.
+        const float *tile = kPooled ? stages + size_t(s) * C::kStageFloats : pool;
+        float relu[C::kGPT];
 #pragma unroll
-            for (int j4 = 0; j4 < F4; ++j4) {
-                const float4 pv = *reinterpret_cast<const float4 *>(pool + pool_index<D>(gl, j4));
-                acc = __fmaf_rn(qreg[4 * j4 + 0], pv.x, acc);
-                acc = __fmaf_rn(qreg[4 * j4 + 1], pv.y, acc);
-                acc = __fmaf_rn(qreg[4 * j4 + 2], pv.z, acc);
-                acc = __fmaf_rn(qreg[4 * j4 + 3], pv.w, acc);
+        for (int i = 0; i < C::kGPT; ++i) {
+            const int g = gl + C::kTG1 * i;
+            relu[i] = 0.0f;
+            if (ok && g < r.n) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int j4 = 0; j4 < F4; ++j4) {
+                    const float4 pv = *reinterpret_cast<const float4 *>(
+                        tile + (kPooled ? g * D + 4 * j4 : pool_index<D>(g, j4)));
+                    acc = __fmaf_rn(qreg[4 * j4 + 0], pv.x, acc);
+                    acc = __fmaf_rn(qreg[4 * j4 + 1], pv.y, acc);
+                    acc = __fmaf_rn(qreg[4 * j4 + 2], pv.z, acc);
+                    acc = __fmaf_rn(qreg[4 * j4 + 3], pv.w, acc);
+                }
+                relu[i] = acc > 0.0f ? acc : 0.0f;
             }
-            relu = acc > 0.0f ? acc : 0.0f;
         }
-        // Head sum, h = 0..H-1 in order, gathered from the H lanes of the group.
+        if constexpr (kPooled) {
+            // the stage has been read by every thread: refill it
+            if (__syncthreads_or(!ok)) {
+                timed_out = true;
+                break;
+            }
+            if (tid == 0) issue(s);
+        }
         const int base = lane & ~(H - 1);
-        float hv[H];
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) hv[hh] = __shfl_sync(0xffffffffu, relu, base + hh);
-        float sum = 0.0f;
+        for (int i = 0; i < C::kGPT; ++i) {
+            const int g = gl + C::kTG1 * i;
+            // Head sum, h = 0..H-1 in order, gathered from the H lanes of the group.
+            float hv[H];
 #pragma unroll
-        for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, hv[hh]);
-        if (h == 0 && gl < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + gl] = sum;
-        // Selection hint: the largest key among groups 4j..4j+3 (the H-lane
-        // blocks of those four groups sit side by side in the warp).
-        uint32_t qk = (gl < r.n) ? order_key(sum) : 0u;
-        qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, H));
-        qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, 2 * H));
-        if ((lane & (4 * H - 1)) == 0 && gl < r.n)
-            a.qmax[int64_t(r.b) * a.qmax_stride + ((r.g0 + gl) >> 2)] = qk;
+            for (int hh = 0; hh < H; ++hh) hv[hh] = __shfl_sync(0xffffffffu, relu[i], base + hh);
+            float sum = 0.0f;
+#pragma unroll
+            for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, hv[hh]);
+            if (h == 0 && g < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + g] = sum;
+            // Selection hint: the largest key among groups 4j..4j+3 (the H-lane
+            // blocks of those four groups sit side by side in the warp).
+            uint32_t qk = (g < r.n) ? order_key(sum) : 0u;
+            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, H));
+            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, 2 * H));
+            if ((lane & (4 * H - 1)) == 0 && g < r.n)
+                a.qmax[int64_t(r.b) * a.qmax_stride + ((r.g0 + g) >> 2)] = qk;
+        }
 
         ++t_cons;
         ++it;

@@ -19,10 +19,10 @@ __all__ = [
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
     "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode",
     "qsa_decode_profiled", "qsa_attend_noalloc", "qsa_pool_groups", "qsa_score_pooled",
-    "qsa_decode_pooled",
+    "qsa_decode_pooled", "qsa_score_groups_shared", "qsa_decode_shared",
     "make_dims",
     "DeviceBatch",
-    "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE",
+    "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE", "QSA_DEVERR_NOT_SHARED",
     "QSA_DEVERR_WAIT_TIMEOUT",
 ]
 
@@ -35,6 +35,7 @@ QSA_DEVERR_VISIBLE_RANGE = 0x1
 QSA_DEVERR_SLOT_RANGE = 0x2
 QSA_DEVERR_ROW_RANGE = 0x4
 QSA_DEVERR_WAIT_TIMEOUT = 0x8
+QSA_DEVERR_NOT_SHARED = 0x10
 
 
 class QsaError(RuntimeError):
@@ -124,6 +125,10 @@ def load(path: str | None = None):
     L.qsa_score_pooled.restype = ctypes.c_int
     L.qsa_decode_pooled.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode_pooled.restype = ctypes.c_int
+    L.qsa_score_groups_shared.argtypes = [_DP, _IP, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_score_groups_shared.restype = ctypes.c_int
+    L.qsa_decode_shared.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_decode_shared.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -299,6 +304,19 @@ def qsa_decode_pooled(dims, inputs, pooled, pool_offset, ids, n_ids, out, ws, st
         _ptr(n_ids), _ptr(out), p, n, _stream(stream)))
 
 
+def qsa_score_groups_shared(dims, inputs, scores, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_score_groups_shared", load().qsa_score_groups_shared(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(scores), p, n, _stream(stream)))
+
+
+def qsa_decode_shared(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
+    p, n = _ws(ws)
+    return _check("qsa_decode_shared", load().qsa_decode_shared(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(out), p, n,
+        _stream(stream)))
+
+
 def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
     """Attention stage with the library's fixed static scratch instead of a
     workspace, for callers that cannot allocate device memory."""
@@ -427,6 +445,13 @@ class DeviceBatch:
     def decode_pooled(self, stream=None):
         return qsa_decode_pooled(self.dims, self.inputs, self.pooled, self.pool_offset, self.ids,
                                  self.n_ids, self.out, self.ws, stream)
+
+    # ---- queries over one shared history ------------------------------------
+    def score_shared(self, stream=None):
+        return qsa_score_groups_shared(self.dims, self.inputs, self.scores, self.ws, stream)
+
+    def decode_shared(self, stream=None):
+        return qsa_decode_shared(self.dims, self.inputs, self.ids, self.n_ids, self.out, self.ws, stream)
 
     def check_errors(self, stream=None):
         return qsa_check_errors(self.ws, stream)
