@@ -249,14 +249,18 @@ qsa_status qsa_decode_profiled(const qsa_dims *dims, const qsa_inputs *in, int32
  * bit, and so do the ID rows and outputs of qsa_decode_pooled.
  *
  * Cache layout (caller-owned, device): pooled[row][d_I] f32; group g of query
- * b lives at row pool_offset[b] + g.  Queries that share a history may share
- * rows (chunked prefill). */
+ * b lives at row pool_offset[b] + g, with its 16-byte chunks permuted within
+ * the row: elements 4c..4c+3 of the pooled key sit at 4(c ^ (g & 7))..+3
+ * (g the query's own group index; d_I is a multiple of 32), so that whole
+ * rows copied into shared memory are read without bank conflicts.  Queries
+ * that share a history may share rows (chunked prefill). */
 
 /* Appends pooled keys: for each query b and g in [group_begin[b],
  * group_end[b]) (device int32 arrays),
- *   pooled[pool_offset[b] + g][j] = (((k0[j]+k1[j])+k2[j])+k3[j]) * 0.25,
+ *   pooled key element j = (((k0[j]+k1[j])+k2[j])+k3[j]) * 0.25,
  *   k_u = idx_keys[key_offset[b] + 4g + u]          (reads in->idx_keys,
- * in->key_offset only).  max_groups (host) bounds group_end[b] -
+ * in->key_offset only), stored at row pool_offset[b] + g in the layout above.
+ * max_groups (host) bounds group_end[b] -
  * group_begin[b] for every b and sizes the launch: a decode step that
  * completes one group per query passes 1.  The caller guarantees the raw rows
  * exist.  A range outside [0, max_visible/4] or longer than max_groups is

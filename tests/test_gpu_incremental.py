@@ -18,6 +18,14 @@ from top_group_sparse_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
+def _logical(rows):
+    """The cache's rows [G, d] with their 16-byte chunks put back in order:
+    chunk c of group g is stored at position c ^ (g & 7)."""
+    G, D = rows.shape
+    idx = np.arange(D // 4)[None, :] ^ (np.arange(G)[:, None] & 7)
+    return np.take_along_axis(rows.reshape(G, D // 4, 4), idx[:, :, None], axis=1).reshape(G, D)
+
+
 def _paged():
     return wl.make_workload("inc", [9001, 2052, 40003, 5, 0], idx_heads=8, idx_dim=64, q_heads=16,
                             kv_heads=2, head_dim=128, seed=71, slots="paged16")
@@ -44,7 +52,7 @@ def test_pooled_cache_matches_oracle_bitwise():
         G = T // 4
         ko = int(w.key_offset[b])
         ref = oracle.pool_cache(w.idx_keys[ko:ko + T], T)
-        got = pooled[po[b]:po[b] + G]
+        got = _logical(pooled[po[b]:po[b] + G])
         assert got.tobytes() == ref.tobytes(), b
 
 

@@ -28,9 +28,10 @@
 //
 // The same kernel scores from a pooled-key cache (the incremental form: the
 // pooled key of every complete group kept in device memory, appended as
-// groups complete): then a stage holds pooled rows, the pooling step becomes
-// a copy into the swizzled tile, and the stream is G * D * 4 bytes per query
-// instead of T * D * 4.  pool_groups_kernel fills that cache with the very
+// groups complete): then a stage holds pooled rows, already in the swizzled
+// tile layout (the cache is stored that way), the dots read the stage in
+// place, and the stream is G * D * 4 bytes per query instead of T * D * 4.
+// pool_groups_kernel fills that cache with the very
 // pooling arithmetic of the raw path (pool4 below), so both forms give the
 // same scores bit for bit -- the full-raw / incremental identity.
 #include "pooling.cuh"
@@ -231,8 +232,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
                 float acc = 0.0f;
 #pragma unroll
                 for (int j4 = 0; j4 < F4; ++j4) {
-                    const float4 pv = *reinterpret_cast<const float4 *>(
-                        tile + (kPooled ? g * D + 4 * j4 : pool_index<D>(g, j4)));
+                    const float4 pv = *reinterpret_cast<const float4 *>(tile + pool_index<D>(g, j4));
                     acc = __fmaf_rn(qreg[4 * j4 + 0], pv.x, acc);
                     acc = __fmaf_rn(qreg[4 * j4 + 1], pv.y, acc);
                     acc = __fmaf_rn(qreg[4 * j4 + 2], pv.z, acc);
@@ -317,7 +317,9 @@ constexpr int kPoolThreads = 256;
 constexpr int kPoolGroupsPerCta = 64;
 
 // pooled[pool_offset[b] + g] = pool of raw rows key_offset[b] + 4g .. 4g+3,
-// for g in [group_begin[b], group_end[b]).  One 16-byte chunk per thread-item.
+// for g in [group_begin[b], group_end[b]).  One 16-byte chunk per thread-item;
+// the row is stored in the pooled-tile layout (chunk j4 at j4 ^ (g & 7)), so a
+// bulk copy of whole rows lands in shared memory ready for conflict-free reads.
 template <int D>
 __global__ void __launch_bounds__(kPoolThreads)
 pool_groups_kernel(const PoolArgs a)
@@ -338,7 +340,7 @@ pool_groups_kernel(const PoolArgs a)
         const int g = g_lo + e / F4;
         const int j4 = e % F4;
         const float4 *k = keys + int64_t(g) * (kGroup * F4) + j4;
-        out[int64_t(g) * F4 + j4] = pool4(__ldg(k), __ldg(k + F4), __ldg(k + 2 * F4), __ldg(k + 3 * F4));
+        out[int64_t(g) * F4 + (j4 ^ (g & 7))] = pool4(__ldg(k), __ldg(k + F4), __ldg(k + 2 * F4), __ldg(k + 3 * F4));
     }
 }
 
