@@ -42,20 +42,21 @@ namespace {
 
 template <int H, int D, bool kPooled>
 struct ScoreCfg {
-    static constexpr int kThreads = 256;
-    // groups per thread per tile: the pooled form moves 4x fewer bytes per
-    // group, so each thread runs four independent FMA chains per tile
-    static constexpr int kGPT = kPooled ? 4 : 1;
+    // The pooled form moves 4x fewer bytes per group, so FMA latency, not
+    // HBM, sets its pace: small CTAs (three per SM) whose threads each run
+    // eight independent FMA chains per tile.
+    static constexpr int kThreads = kPooled ? 128 : 256;
+    static constexpr int kGPT = kPooled ? 8 : 1;            // groups per thread per tile
     static constexpr int kTG1 = kThreads / H;               // groups per pass of the CTA
     static constexpr int kTG = kTG1 * kGPT;                 // groups per tile
     static constexpr int kGroupFloats = kPooled ? D : kGroup * D;  // stage floats per group
     static constexpr int kStageFloats = kTG * kGroupFloats;
     static constexpr int kStageBytes = kStageFloats * 4;
-    // Two CTAs per SM when a stage is small enough, so that one CTA's
+    // Raw: two CTAs per SM when a stage is small enough, so that one CTA's
     // barriers and FMA chains overlap the other's; ~96-192 KB of raw keys in
-    // flight per SM either way.
-    static constexpr int kCtasPerSm = kStageBytes <= 32768 ? 2 : 1;
-    static constexpr int kStageBudget = kCtasPerSm == 2 ? 98304 : 196608;
+    // flight per SM either way.  Pooled: three CTAs of 64 KB of stages.
+    static constexpr int kCtasPerSm = kPooled ? (kStageBytes <= 32768 ? 3 : 1) : (kStageBytes <= 32768 ? 2 : 1);
+    static constexpr int kStageBudget = kCtasPerSm == 3 ? 65536 : (kCtasPerSm == 2 ? 98304 : 196608);
     static constexpr int kStagesRaw = kStageBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     // one pooled tile (swizzled), double buffered; the pooled form reads its
@@ -223,24 +224,30 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
         // Dots: groups gl + kTG1 * i of the tile, i < kGPT, each a D-long chain.
         const float *tile = kPooled ? stages + size_t(s) * C::kStageFloats : pool;
-        float relu[C::kGPT];
+        // The kGPT chains advance side by side (independent FMAs to overlap);
+        // rows past the tile's end compute from stale shared memory and are
+        // dropped below.
+        float acc[C::kGPT];
 #pragma unroll
-        for (int i = 0; i < C::kGPT; ++i) {
-            const int g = gl + C::kTG1 * i;
-            relu[i] = 0.0f;
-            if (ok && g < r.n) {
-                float acc = 0.0f;
+        for (int i = 0; i < C::kGPT; ++i) acc[i] = 0.0f;
 #pragma unroll
-                for (int j4 = 0; j4 < F4; ++j4) {
-                    const float4 pv = *reinterpret_cast<const float4 *>(tile + pool_index<D>(g, j4));
-                    acc = __fmaf_rn(qreg[4 * j4 + 0], pv.x, acc);
-                    acc = __fmaf_rn(qreg[4 * j4 + 1], pv.y, acc);
-                    acc = __fmaf_rn(qreg[4 * j4 + 2], pv.z, acc);
-                    acc = __fmaf_rn(qreg[4 * j4 + 3], pv.w, acc);
-                }
-                relu[i] = acc > 0.0f ? acc : 0.0f;
+        for (int j4 = 0; j4 < F4; ++j4) {
+            float4 pv[C::kGPT];
+#pragma unroll
+            for (int i = 0; i < C::kGPT; ++i)
+                pv[i] = *reinterpret_cast<const float4 *>(tile + pool_index<D>(gl + C::kTG1 * i, j4));
+#pragma unroll
+            for (int i = 0; i < C::kGPT; ++i) {
+                acc[i] = __fmaf_rn(qreg[4 * j4 + 0], pv[i].x, acc[i]);
+                acc[i] = __fmaf_rn(qreg[4 * j4 + 1], pv[i].y, acc[i]);
+                acc[i] = __fmaf_rn(qreg[4 * j4 + 2], pv[i].z, acc[i]);
+                acc[i] = __fmaf_rn(qreg[4 * j4 + 3], pv[i].w, acc[i]);
             }
         }
+        float relu[C::kGPT];
+#pragma unroll
+        for (int i = 0; i < C::kGPT; ++i)
+            relu[i] = (ok && gl + C::kTG1 * i < r.n && acc[i] > 0.0f) ? acc[i] : 0.0f;
         if constexpr (kPooled) {
             // the stage has been read by every thread: refill it
             if (__syncthreads_or(!ok)) {
