@@ -222,18 +222,21 @@ int32_t qsao_resolve(const int32_t *ids, int32_t n, const int32_t *slot_map,
 
 /* ---- 7. attend ---------------------------------------------------------- */
 
-/* q: [n_q, d]; k_cache, v_cache: [num_slots, n_kv, d]; slots[0..n) in
- * emitted order; out: [n_q, d].  Sequential online softmax, one visit per
- * row, in the given order. */
-void qsao_attend(const float *q, int32_t n_q, int32_t n_kv, int32_t d, float scale,
-                 const float *k_cache, const float *v_cache,
-                 const int32_t *slots, int32_t n, float *out)
+/* The online-softmax state after visiting rows slots[0..n) in the given
+ * order, for every q head h: m_out[h] the running maximum (-inf before any
+ * row), l_out[h] the denominator, acc_out[h][0..d) the unnormalised output.
+ * q: [n_q, d]; k_cache, v_cache: [num_slots, n_kv, d].  Sequential, one
+ * visit per row. */
+void qsao_attend_partial(const float *q, int32_t n_q, int32_t n_kv, int32_t d, float scale,
+                         const float *k_cache, const float *v_cache,
+                         const int32_t *slots, int32_t n,
+                         float *m_out, float *l_out, float *acc_out)
 {
     int32_t group = n_q / n_kv;
-    float *acc = (float *)malloc(sizeof(float) * (size_t)d);
     for (int32_t h = 0; h < n_q; ++h) {
         int32_t kvh = h / group;
         const float *qh = q + (int64_t)h * d;
+        float *acc = acc_out + (int64_t)h * d;
         float m = -INFINITY, l = 0.0f;
         for (int32_t j = 0; j < d; ++j) acc[j] = 0.0f;
         for (int32_t i = 0; i < n; ++i) {
@@ -249,10 +252,28 @@ void qsao_attend(const float *q, int32_t n_q, int32_t n_kv, int32_t d, float sca
             for (int32_t j = 0; j < d; ++j) acc[j] = acc[j] * alpha + p * v[j];
             m = m_new;
         }
+        m_out[h] = m;
+        l_out[h] = l;
+    }
+}
+
+/* out: [n_q, d] = acc / l of the state above (0 for an empty row): the
+ * attention of the q heads over the rows in the given order. */
+void qsao_attend(const float *q, int32_t n_q, int32_t n_kv, int32_t d, float scale,
+                 const float *k_cache, const float *v_cache,
+                 const int32_t *slots, int32_t n, float *out)
+{
+    float *m = (float *)malloc(sizeof(float) * (size_t)(n_q > 0 ? n_q : 1));
+    float *l = (float *)malloc(sizeof(float) * (size_t)(n_q > 0 ? n_q : 1));
+    float *acc = (float *)malloc(sizeof(float) * (size_t)(n_q > 0 ? n_q : 1) * (size_t)d);
+    qsao_attend_partial(q, n_q, n_kv, d, scale, k_cache, v_cache, slots, n, m, l, acc);
+    for (int32_t h = 0; h < n_q; ++h) {
         float *o = out + (int64_t)h * d;
-        for (int32_t j = 0; j < d; ++j) o[j] = l > 0.0f ? acc[j] / l : 0.0f;
+        for (int32_t j = 0; j < d; ++j) o[j] = l[h] > 0.0f ? acc[(int64_t)h * d + j] / l[h] : 0.0f;
     }
     free(acc);
+    free(l);
+    free(m);
 }
 
 /* ---- whole decode over a batch ------------------------------------------ */

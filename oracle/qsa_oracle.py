@@ -22,7 +22,7 @@ import numpy as np
 __all__ = [
     "build", "lib", "num_groups", "tail_len", "row_width", "pool_group",
     "score_groups", "score_groups_incremental", "pool_cache", "select", "dense_ids",
-    "resolve", "attend", "decode", "GROUP",
+    "resolve", "attend", "attend_partial", "decode", "GROUP",
 ]
 
 GROUP = 4
@@ -98,6 +98,9 @@ def _declare(L):
     L.qsao_resolve.restype = _i32
     L.qsao_attend.argtypes = [_F32P, _i32, _i32, _i32, _f32, _F32P, _F32P, _I32P, _i32, _F32P]
     L.qsao_attend.restype = None
+    L.qsao_attend_partial.argtypes = [_F32P, _i32, _i32, _i32, _f32, _F32P, _F32P, _I32P, _i32,
+                                      _F32P, _F32P, _F32P]
+    L.qsao_attend_partial.restype = None
     L.qsao_decode.argtypes = [
         _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
         _F32P, _F32P, _I64P, _I32P, _F32P, _F32P, _F32P, _i64, _I32P, _I64P,
@@ -242,6 +245,25 @@ def attend(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     lib().qsao_attend(pq, n_q, n_kv, d, float(scale), pk, pv, ps, len(slots),
                       out.ctypes.data_as(_F32P))
     return out
+
+
+def attend_partial(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                   slots: np.ndarray, scale: float):
+    """The online-softmax state (m [n_q], l [n_q], acc [n_q, d]) after the
+    rows `slots` in order; attend() is acc / l of it."""
+    q, pq = _fa(q)
+    k_cache, pk = _fa(k_cache)
+    v_cache, pv = _fa(v_cache)
+    slots, ps = _ia(slots)
+    n_q, d = q.shape
+    n_kv = k_cache.shape[1]
+    m = np.empty(n_q, np.float32)
+    l = np.empty(n_q, np.float32)
+    acc = np.empty((n_q, d), np.float32)
+    lib().qsao_attend_partial(pq, n_q, n_kv, d, float(scale), pk, pv, ps, len(slots),
+                              m.ctypes.data_as(_F32P), l.ctypes.data_as(_F32P),
+                              acc.ctypes.data_as(_F32P))
+    return m, l, acc
 
 
 def decode(w, with_scores: bool = False, queries=None):

@@ -1,4 +1,5 @@
-"""Query sharding across GPUs (host logic only).
+"""Sharding across GPUs (host logic only): a batch by query, or one long
+history by group ranges.
 
 Decode queries are independent, so a batch splits across ranks by query with
 no exchange on the data path; the only collective is the harness's
@@ -26,3 +27,108 @@ def max_over_ranks(value: float, device=None) -> float:
     t = torch.tensor([float(value)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# ---- one long sequence across ranks ------------------------------------------
+#
+# "Top-k chooses the set; time chooses the order" (AFN-017) and "A sparse mask
+# is not sparse attention" (AFN-016) define the path for one query over its
+# whole history.  When one history is split across ranks by contiguous ranges
+# of complete groups (rank r holds groups [g_lo, g_hi) and, on the last rank,
+# the raw tail), the path needs exactly one exchange:
+#   1. each rank scores its groups and keeps its local top min(budget, n_r)
+#      by (score descending, position ascending) -- every group of the global
+#      set is in its own rank's local set, because the local order is the
+#      global order restricted to the rank's groups;
+#   2. the candidates are exchanged (all-gather of at most budget per rank)
+#      and every rank merges them with the same rule: the chosen set, ties
+#      decided during membership exactly as on one device;
+#   3. the emitted row (chosen groups ascending, x4, then the tail) is the same
+#      on every rank; the rows of rank r form one contiguous slice of it, and
+#      rank order is time order;
+#   4. each rank runs the online softmax over its slice, in order, and the
+#      per-rank states (m, l, acc) are merged in ascending rank order.
+
+
+def shard_groups(n_groups: int, world: int, rank: int) -> range:
+    """Contiguous, balanced share of groups 0..n_groups-1 for `rank`."""
+    return shard_queries(n_groups, world, rank)
+
+
+def order_keys(scores) -> "np.ndarray":
+    """Order-preserving uint32 images of scores in [+0, +inf] (-0 read as +0)."""
+    import numpy as np
+    s = np.asarray(scores, dtype=np.float32)
+    if s.size and (np.isnan(s).any() or (s < 0).any()):
+        raise ValueError("scores must lie in [+0, +inf]")
+    s = np.where(s == 0, np.float32(0.0), s).astype(np.float32)
+    return s.view(np.uint32)
+
+
+def _rank_order(keys, groups):
+    """Indices ordering (key, group) by key descending, then group ascending."""
+    import numpy as np
+    return np.lexsort((np.asarray(groups, np.int64), -np.asarray(keys, np.int64)))
+
+
+def local_candidates(scores, g_lo: int, budget: int):
+    """This rank's top min(budget, n) groups of scores[0..n) (groups g_lo +
+    i) as (keys uint32, groups int64), best first."""
+    import numpy as np
+    keys = order_keys(scores)
+    groups = np.arange(g_lo, g_lo + keys.size, dtype=np.int64)
+    take = _rank_order(keys, groups)[:min(budget, keys.size)]
+    return keys[take], groups[take]
+
+
+def merge_candidates(parts, budget: int, n_groups: int):
+    """The chosen set of the whole history, ascending, from every rank's
+    local candidates (any rank order)."""
+    import numpy as np
+    keys = np.concatenate([np.asarray(p[0], np.uint32) for p in parts]) if parts else np.zeros(0, np.uint32)
+    groups = np.concatenate([np.asarray(p[1], np.int64) for p in parts]) if parts else np.zeros(0, np.int64)
+    k = min(budget, n_groups)
+    if groups.size < k:
+        raise ValueError("fewer candidates than the budget: a rank sent too few")
+    return np.sort(groups[_rank_order(keys, groups)[:k]])
+
+
+def emitted_row(chosen, T: int):
+    """Chosen groups (ascending) expanded to 4 token IDs each, then the raw
+    tail [4 * floor(T/4), T): the row every rank holds."""
+    import numpy as np
+    chosen = np.asarray(chosen, np.int64)
+    body = (4 * chosen[:, None] + np.arange(4, dtype=np.int64)[None, :]).reshape(-1)
+    tail = np.arange(4 * (T // 4), T, dtype=np.int64)
+    return np.concatenate([body, tail]).astype(np.int32)
+
+
+def rank_rows(ids, g_lo: int, g_hi: int, last: bool) -> slice:
+    """The contiguous slice of the emitted row owned by the rank holding
+    groups [g_lo, g_hi) (and the tail, when it is the last rank)."""
+    import numpy as np
+    ids = np.asarray(ids, np.int64)
+    start = int(np.searchsorted(ids, 4 * g_lo, side="left"))
+    stop = ids.size if last else int(np.searchsorted(ids, 4 * g_hi, side="left"))
+    return slice(start, stop)
+
+
+def merge_partials(parts):
+    """Output [n_q, d] from per-rank online-softmax states (m [n_q], l [n_q],
+    acc [n_q, d]) given in ascending rank (time) order; binary32 throughout,
+    an empty state (m = -inf, l = 0) contributes nothing, an empty row gives 0."""
+    import numpy as np
+    m = np.array(parts[0][0], np.float32)
+    l = np.array(parts[0][1], np.float32)
+    acc = np.array(parts[0][2], np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        for m2, l2, a2 in parts[1:]:
+            m2 = np.asarray(m2, np.float32)
+            mn = np.maximum(m, m2)
+            s1 = np.where(m == -np.inf, np.float32(0.0), np.exp(m - mn)).astype(np.float32)
+            s2 = np.where(m2 == -np.inf, np.float32(0.0), np.exp(m2 - mn)).astype(np.float32)
+            l = (l * s1 + np.asarray(l2, np.float32) * s2).astype(np.float32)
+            acc = (acc * s1[:, None] + np.asarray(a2, np.float32) * s2[:, None]).astype(np.float32)
+            m = mn
+        out = np.where(l[:, None] > 0, acc / np.where(l > 0, l, np.float32(1.0))[:, None], np.float32(0.0))
+    return out.astype(np.float32)
