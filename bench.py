@@ -82,6 +82,28 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def ffma_peak(stream):
+    """Binary32 FFMA rate of this GPU from the library's probe
+    (qsa_probe_ffma): best of 5 event-timed launches after 2 warm-ups."""
+    import torch
+    from top_group_sparse_gb300 import qsa
+    bps, iters = 4, 256
+    sink = torch.zeros(1 << 14, dtype=torch.float32, device="cuda")
+    best = float("inf")
+    n_fma = 0
+    for r in range(7):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n_fma = qsa.qsa_probe_ffma(bps, iters, sink, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if r >= 2:
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+    return {"tflops": 2 * n_fma / best / 1e12,
+            "how": f"qsa_probe_ffma, {bps} x 256 threads per SM, 8 chains x {16 * iters} FMAs per thread, "
+                   "best of 5 launches"}
+
+
 def profile_traffic():
     """Per-launch DRAM bytes of the scorer from the committed ncu summary, or
     None if it is missing or was taken on a different scorer source."""
@@ -164,6 +186,7 @@ def run_reference(args):
     import oracle
     from top_group_sparse_gb300 import workloads as wl
     w = wl.long_262144(batch=args.batch)
+    n_thr = oracle.threads(os.cpu_count() or 1)  # every host core (1 if built without OpenMP)
     t0 = time.perf_counter()
     oracle.decode(w, queries=[0])
     per_query = time.perf_counter() - t0
@@ -182,9 +205,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": config_dict(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n_thr, "kind": "oracle",
                          "sample": f"{per_step} of the {w.batch} queries of the batch per step, "
-                                   f"single-threaded plain C oracle"},
+                                   f"plain C oracle on {n_thr} host threads (OpenMP over queries, "
+                                   f"groups and heads; results identical to one thread)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -365,12 +389,31 @@ def run_gpu(args):
 
         ms_shared = time_path(dc.decode_shared)
         ms_single = time_path(dc.decode)
+        ms_scorer = time_path(dc.score_shared)
         st, flags = dc.check_errors()
         if st != 0:
             raise SystemExit(f"device error word {flags:#x} in the chunked-prefill loop")
+        # This workload is FFMA-bound (one key history, 256 queries): its
+        # roofline denominator is the FFMA rate measured here by the library's
+        # probe, beside the HBM one.
+        ffma = ffma_peak(stream)
+        Gs = wc.visible // 4
+        Ws = 4 * np.minimum(Gs, wc.budget) + wc.visible % 4
+        fma_score = int(np.sum(Gs.astype(np.int64)) * wc.idx_heads * wc.idx_dim)
+        fma_attend = int(np.sum(Ws.astype(np.int64)) * wc.q_heads * wc.head_dim * 2)
+        key_bytes = int(wc.visible.max()) * wc.idx_dim * 4  # the shared history, streamed once
         chunk = {"workload": "chunked_prefill_100000", "queries_per_step": wc.batch,
                  "shared": {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared},
                  "per_query": {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single},
+                 "roofline": {"bound": "alu", "kernel": "score_shared_kernel (qsa_score_groups_shared)",
+                              "achieved": 2 * fma_score / (ms_scorer * 1e-3) / 1e12,
+                              "peak": ffma["tflops"], "unit": "TFLOP/s",
+                              "frac": 2 * fma_score / (ms_scorer * 1e-3) / 1e12 / ffma["tflops"],
+                              "us_per_launch": ms_scorer * 1e3, "fma_per_launch": fma_score,
+                              "peak_source": "measured in this run: " + ffma["how"],
+                              "hbm_frac": key_bytes / (ms_scorer * 1e-3) / 1e9 / measured_peaks()[0],
+                              "step_fma": fma_score + fma_attend,
+                              "step_frac": 2 * (fma_score + fma_attend) / (ms_shared * 1e-3) / 1e12 / ffma["tflops"]},
                  "note": "256 queries at positions 100,000..100,255 of one history: qsa_decode_shared "
                          "(each pooled tile scored for every query) vs qsa_decode (each query streams "
                          "its own keys); outputs bit-identical (tests); L2 flushed before each step"}
@@ -428,17 +471,26 @@ def run_gpu(args):
     if ws == 1 and not args.no_cpu_baseline:
         import oracle
         sample = list(range(w.batch))
-        t0 = time.perf_counter()
-        reps = 0
-        while True:
-            oracle.decode(w, queries=sample)
-            reps += 1
-            if time.perf_counter() - t0 > 8.0 or reps >= 4:
-                break
-        dt = time.perf_counter() - t0
-        cpu = {"value": reps * len(sample) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{reps} pass(es) over all {len(sample)} queries of the batch, "
-                         f"single-threaded plain C oracle, {dt:.1f} s"}
+
+        def time_oracle(n_threads):
+            n = oracle.threads(n_threads)
+            t0 = time.perf_counter()
+            reps = 0
+            while True:  # about 10-16 s of host-thread time, at least 4 passes
+                oracle.decode(w, queries=sample)
+                reps += 1
+                el = time.perf_counter() - t0
+                if reps >= 4 and (el * n >= 10.0 or el >= 12.0):
+                    break
+            dt = time.perf_counter() - t0
+            return {"value": reps * len(sample) / dt, "unit": UNIT, "cores": n, "kind": "oracle",
+                    "sample": f"{reps} pass(es) over all {len(sample)} queries of the batch, plain C "
+                              f"oracle on {n} host thread(s), {dt:.1f} s"}
+
+        # every host core (OpenMP over queries, groups and heads: the same
+        # results as one thread), and one thread
+        cpu = time_oracle(os.cpu_count() or 1)
+        cpu_1t = time_oracle(1)
 
     clocks = clk.summary()
     line = {
@@ -475,6 +527,7 @@ def run_gpu(args):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        line["cpu_baseline_1thread"] = cpu_1t
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -331,6 +331,18 @@ qsa_status qsa_decode_shared(const qsa_dims *dims, const qsa_inputs *in, int32_t
 qsa_status qsa_attend_noalloc(const qsa_dims *dims, const float *q, const float *k_scr,
                               const float *v_scr, const int32_t *n_ids, float *out, void *stream);
 
+/* ---- measurement -------------------------------------------------------- */
+
+/* Launches a binary32 FFMA throughput probe on `stream`: blocks_per_sm (1..8)
+ * blocks of 256 threads per SM, each thread running 8 independent FMA chains
+ * for iters x 16 steps; *fma_count (host) receives the FMAs the launch
+ * performs.  The caller times it (events on `stream`): 2 * fma_count / time
+ * is the FFMA peak that an FFMA-bound kernel of this library is reported
+ * against.  sink: >= sms * blocks_per_sm floats of device memory, written
+ * only to keep the chains from being optimised away (in practice never). */
+qsa_status qsa_probe_ffma(int32_t blocks_per_sm, int32_t iters, float *sink, int64_t *fma_count,
+                          void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define QSAO_GROUP 4
 
@@ -110,17 +113,40 @@ float qsao_score_pooled(const float *q, int32_t H, int32_t d, const float *p)
 }
 
 /* Full-raw scoring: keys [T, d] are the query's raw index keys in logical
- * order; writes scores[0..G). */
+ * order; writes scores[0..G).  Each group's score depends on that group
+ * alone, so when built with OpenMP the groups are shared out among the host
+ * threads (same arithmetic per group, same results). */
 void qsao_score_groups(const float *q, int32_t H, int32_t d, const float *keys,
                        int32_t T, float pool_scale, float *scores)
 {
     int32_t G = qsao_num_groups(T);
-    float *p = (float *)malloc(sizeof(float) * (size_t)(d > 0 ? d : 1));
-    for (int32_t g = 0; g < G; ++g) {
-        qsao_pool_group(keys + (int64_t)g * QSAO_GROUP * d, d, pool_scale, p);
-        scores[g] = qsao_score_pooled(q, H, d, p);
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        float *p = (float *)malloc(sizeof(float) * (size_t)(d > 0 ? d : 1));
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+        for (int32_t g = 0; g < G; ++g) {
+            qsao_pool_group(keys + (int64_t)g * QSAO_GROUP * d, d, pool_scale, p);
+            scores[g] = qsao_score_pooled(q, H, d, p);
+        }
+        free(p);
     }
-    free(p);
+}
+
+/* Host threads the scoring uses (1 without OpenMP); n <= 0 keeps the current
+ * setting.  Returns the setting in force. */
+int32_t qsao_threads(int32_t n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return (int32_t)omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }
 
 /* Incremental pooled-key cache ([AFN-017] Retrieval capsule names
@@ -233,6 +259,10 @@ void qsao_attend_partial(const float *q, int32_t n_q, int32_t n_kv, int32_t d, f
                          float *m_out, float *l_out, float *acc_out)
 {
     int32_t group = n_q / n_kv;
+    /* heads are independent: shared among host threads under OpenMP */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int32_t h = 0; h < n_q; ++h) {
         int32_t kvh = h / group;
         const float *qh = q + (int64_t)h * d;
@@ -296,12 +326,31 @@ int32_t qsao_decode(int32_t B, int32_t H, int32_t dI, int32_t n_q, int32_t n_kv,
                     float *scores, int32_t gstride,
                     int32_t *ids, int32_t row_cap, int32_t *n_ids, float *out)
 {
-    int32_t status = 0;
     for (int32_t b = 0; b < B; ++b) {
         int32_t T = visible[b];
-        int32_t G = qsao_num_groups(T);
-        if (T < 0 || qsao_row_width(T, budget) > row_cap || (scores && G > gstride))
+        if (T < 0 || qsao_row_width(T, budget) > row_cap ||
+            (scores && qsao_num_groups(T) > gstride))
             return -1;
+    }
+    /* Queries are independent: under OpenMP they are shared among the host
+     * threads, and the threads left over (fewer queries than threads) share
+     * each query's groups and heads one level down.  Per-query results are
+     * those of the sequential loop. */
+    int32_t *st_b = (int32_t *)calloc((size_t)(B > 0 ? B : 1), sizeof(int32_t));
+#ifdef _OPENMP
+    int n_thr = omp_get_max_threads();
+    int outer = B < n_thr ? (B > 0 ? B : 1) : n_thr;
+    int inner = n_thr / outer > 0 ? n_thr / outer : 1;
+    int levels = omp_get_max_active_levels();
+    omp_set_max_active_levels(2);
+#pragma omp parallel for num_threads(outer) schedule(dynamic, 1)
+#endif
+    for (int32_t b = 0; b < B; ++b) {
+#ifdef _OPENMP
+        omp_set_num_threads(inner);
+#endif
+        int32_t T = visible[b];
+        int32_t G = qsao_num_groups(T);
         float *sc = (float *)malloc(sizeof(float) * (size_t)(G > 0 ? G : 1));
         qsao_score_groups(q_idx + (int64_t)b * H * dI, H, dI,
                           idx_keys + key_offset[b] * dI, T, 0.25f, sc);
@@ -314,7 +363,7 @@ int32_t qsao_decode(int32_t B, int32_t H, int32_t dI, int32_t n_q, int32_t n_kv,
         float *ob = out + (int64_t)b * n_q * hd;
         if (qsao_resolve(row, n, slot_map + slot_offset[b], num_slots, slots) != 0) {
             for (int64_t e = 0; e < (int64_t)n_q * hd; ++e) ob[e] = 0.0f;
-            if (status == 0) status = 1 + b;
+            st_b[b] = 1;
         } else {
             qsao_attend(q + (int64_t)b * n_q * hd, n_q, n_kv, hd, scale,
                         k_cache, v_cache, slots, n, ob);
@@ -322,5 +371,12 @@ int32_t qsao_decode(int32_t B, int32_t H, int32_t dI, int32_t n_q, int32_t n_kv,
         free(slots);
         free(sc);
     }
+#ifdef _OPENMP
+    omp_set_max_active_levels(levels);
+#endif
+    int32_t status = 0;
+    for (int32_t b = 0; b < B && status == 0; ++b)
+        if (st_b[b]) status = 1 + b;
+    free(st_b);
     return status;
 }

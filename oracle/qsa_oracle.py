@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 import platform
+import shutil
 import subprocess
 import tempfile
 
@@ -22,7 +23,7 @@ import numpy as np
 __all__ = [
     "build", "lib", "num_groups", "tail_len", "row_width", "pool_group",
     "score_groups", "score_groups_incremental", "pool_cache", "select", "dense_ids",
-    "resolve", "attend", "attend_partial", "decode", "GROUP",
+    "resolve", "attend", "attend_partial", "decode", "threads", "GROUP",
 ]
 
 GROUP = 4
@@ -36,11 +37,32 @@ _lib = None
 
 def _cflags() -> list[str]:
     flags = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+    if _has_openmp():
+        flags.append("-fopenmp")  # the per-group scoring loop, shared among host threads
     # fmaf() is correctly rounded by definition; on x86-64 the FMA extension
     # only turns the libm call into one instruction with the same result.
     if platform.machine() in ("x86_64", "AMD64"):
         flags.append("-mfma")
     return flags
+
+
+def _has_openmp() -> bool:
+    """Whether gcc here builds and links OpenMP code."""
+    global _omp
+    if _omp is None:
+        d = tempfile.mkdtemp()
+        try:
+            c = os.path.join(d, "t.c")
+            open(c, "w").write("#include <omp.h>\nint f(void){return omp_get_max_threads();}\n")
+            r = subprocess.run(["gcc", "-fopenmp", "-fPIC", "-shared", c, "-o", os.path.join(d, "t.so")],
+                               capture_output=True)
+            _omp = r.returncode == 0
+        finally:
+            shutil.rmtree(d, ignore_errors=True)
+    return _omp
+
+
+_omp = None
 
 
 def build(force: bool = False, sanitize: bool = False, out: str | None = None,
@@ -52,8 +74,8 @@ def build(force: bool = False, sanitize: bool = False, out: str | None = None,
         return so
     os.makedirs(os.path.dirname(so), exist_ok=True)
     flags = _cflags()
-    if sanitize:
-        flags = [f for f in flags if f != "-O2"] + [
+    if sanitize:  # (single-threaded: the sanitizers see the plain loops)
+        flags = [f for f in flags if f not in ("-O2", "-fopenmp")] + [
             "-O1", "-g", "-fsanitize=address,undefined", "-fno-omit-frame-pointer",
             "-fno-sanitize-recover=all"]
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(so))
@@ -98,6 +120,8 @@ def _declare(L):
     L.qsao_resolve.restype = _i32
     L.qsao_attend.argtypes = [_F32P, _i32, _i32, _i32, _f32, _F32P, _F32P, _I32P, _i32, _F32P]
     L.qsao_attend.restype = None
+    L.qsao_threads.argtypes = [_i32]
+    L.qsao_threads.restype = _i32
     L.qsao_attend_partial.argtypes = [_F32P, _i32, _i32, _i32, _f32, _F32P, _F32P, _I32P, _i32,
                                       _F32P, _F32P, _F32P]
     L.qsao_attend_partial.restype = None
@@ -245,6 +269,11 @@ def attend(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     lib().qsao_attend(pq, n_q, n_kv, d, float(scale), pk, pv, ps, len(slots),
                       out.ctypes.data_as(_F32P))
     return out
+
+
+def threads(n: int = 0) -> int:
+    """Host threads the scoring loop uses (n > 0 sets it); 1 without OpenMP."""
+    return int(lib().qsao_threads(int(n)))
 
 
 def attend_partial(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,

@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 20
+    assert len(names) == 21
     for n in names:
         assert hasattr(lib, n), n
     for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",
@@ -134,3 +134,10 @@ def test_validation_rejects_before_launch(lib):
     assert _raw("qsa_attend", D(d), fake, fake, fake, fake, fake, fake, 100, None) == WS_SMALL
     assert _raw("qsa_workspace_init", None, 10, None) == INVALID
     assert _raw("qsa_check_errors", fake, 8, None, None) == INVALID
+
+
+def test_ffma_probe_rejects_bad_arguments(lib):
+    """Checked on the host before any launch: no GPU needed."""
+    for bps, iters in ((0, 10), (9, 10), (4, 0)):
+        with pytest.raises(qsa.QsaError):
+            qsa.qsa_probe_ffma(bps, iters, None, stream=0)

@@ -476,3 +476,23 @@ def test_budget_one_and_small_budgets(oracle):
         _, chosen = oracle.select(s, 4 * 50 + 1, k, return_chosen=True)
         order = sorted(range(50), key=lambda g: (-float(s[g]), g))[:min(k, 50)]
         assert chosen.tolist() == sorted(order)
+
+
+def test_oracle_threads_do_not_change_results():
+    """The oracle's OpenMP loops (queries, groups, heads) share out
+    independent work only: any thread count gives the one-thread bytes."""
+    import oracle
+    from top_group_sparse_gb300 import workloads as wl
+    w = wl.make_workload("thr", [9001, 37, 2052, 4 * 700 + 3, 0], idx_heads=4, idx_dim=32, q_heads=4,
+                         kv_heads=2, head_dim=64, seed=23, slots="paged16")
+    before = oracle.threads()
+    try:
+        oracle.threads(1)
+        one = oracle.decode(w, with_scores=True)
+        for n in (2, 3, 8):
+            oracle.threads(n)
+            many = oracle.decode(w, with_scores=True)
+            for k in ("ids", "n_ids", "out", "scores"):
+                assert many[k].tobytes() == one[k].tobytes(), (n, k)
+    finally:
+        oracle.threads(before)

@@ -19,7 +19,7 @@ __all__ = [
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
     "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode",
     "qsa_decode_profiled", "qsa_attend_noalloc", "qsa_pool_groups", "qsa_score_pooled",
-    "qsa_decode_pooled", "qsa_score_groups_shared", "qsa_decode_shared",
+    "qsa_decode_pooled", "qsa_score_groups_shared", "qsa_decode_shared", "qsa_probe_ffma",
     "make_dims",
     "DeviceBatch",
     "QSA_DEVERR_VISIBLE_RANGE", "QSA_DEVERR_SLOT_RANGE", "QSA_DEVERR_ROW_RANGE", "QSA_DEVERR_NOT_SHARED",
@@ -129,6 +129,8 @@ def load(path: str | None = None):
     L.qsa_score_groups_shared.restype = ctypes.c_int
     L.qsa_decode_shared.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode_shared.restype = ctypes.c_int
+    L.qsa_probe_ffma.argtypes = [ctypes.c_int32, ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_int64), _P]
+    L.qsa_probe_ffma.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -315,6 +317,14 @@ def qsa_decode_shared(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
     return _check("qsa_decode_shared", load().qsa_decode_shared(
         ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(out), p, n,
         _stream(stream)))
+
+
+def qsa_probe_ffma(blocks_per_sm, iters, sink, stream=None) -> int:
+    """Launches the FFMA throughput probe; returns the FMAs it performs."""
+    count = ctypes.c_int64(0)
+    _check("qsa_probe_ffma", load().qsa_probe_ffma(int(blocks_per_sm), int(iters), _ptr(sink),
+                                                   ctypes.byref(count), _stream(stream)))
+    return int(count.value)
 
 
 def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
