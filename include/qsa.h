@@ -122,7 +122,9 @@ typedef struct {
 /* Bytes of workspace every call below needs for these dims (0 if the dims
  * are invalid).  Sized as groups + budget + selected width per query,
  * never queries x keys ([AFN-016] What the checkpoint measures):
- *   header + B*score_stride*4 (scores) + B*qstride*4 (the largest score of
+ *   header (256 + align256(B*n_kv*4) attention tickets + 7,424 for the
+ *   scorer's per-SM balance: weights learned from its own timings) +
+ *   B*score_stride*4 (scores) + B*qstride*4 (the largest score of
  *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
  *   to 32, G_max = max_visible/4) +
  *   B*n_q*9*(d+2)*4 (attention partials: 9 runs of 256 rows per head).
@@ -165,7 +167,11 @@ qsa_status qsa_check_errors(void *ws, size_t ws_bytes, void *stream, uint32_t *f
  *   dot_h = fma chain over j = 0..d_I-1 starting from +0, ReLU(x) = x>0 ? x : +0,
  * every step binary32 round-to-nearest in exactly that order, so scores are
  * bit-identical to any implementation of that order.
- * scores: [B, qsa_score_stride(dims)]; entries g >= floor(T_b/4) untouched. */
+ * scores: [B, qsa_score_stride(dims)]; entries g >= floor(T_b/4) untouched.
+ * When the tiles fill every SM, the launch is cooperative and each SM's
+ * share of the tiles follows its streaming speed as measured in earlier
+ * launches on this workspace (the weights qsa_decode keeps up to date); the
+ * shares move work between SMs and never change a score. */
 qsa_status qsa_score_groups(const qsa_dims *dims, const qsa_inputs *in, float *scores,
                             void *ws, size_t ws_bytes, void *stream);
 
@@ -225,7 +231,9 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
  * zero dense-mask bytes) -- each attention CTA copies its selected K/V rows
  * from the cache straight into shared memory, so the compact row is never
  * written to device memory.  Outputs: ids, n_ids (as qsa_select) and out,
- * bit-identical to qsa_attend over qsa_gather's scratch. */
+ * bit-identical to qsa_attend over qsa_gather's scratch.  The selection
+ * launch has one spare CTA that turns the scorer's recorded times into its
+ * per-SM shares for the next call on this workspace. */
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 

@@ -234,3 +234,33 @@ def test_decode_profiled_matches_decode():
     gpu = {"ids": db.ids.cpu().numpy(), "n_ids": db.n_ids.cpu().numpy(), "out": db.out.cpu().numpy()}
     assert_ids_equal(w, gpu, ref)
     assert_attention_close(w, gpu, ref)
+
+
+def test_per_sm_balance_engages_and_leaves_results_unchanged():
+    """The raw scorer's per-SM shares (weights learned from its own timings,
+    kept in the workspace) move tiles between SMs and nothing else: the
+    first decode on a fresh workspace (equal shares) and later ones
+    (weighted shares) give the same rows and outputs bit for bit, and the
+    weights are in place after the first decode."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    w = wl.long_262144(batch=2)
+    db = qsa.DeviceBatch(w)
+    db.decode()
+    torch.cuda.synchronize()
+    ids, out = db.ids.cpu().numpy().copy(), db.out.cpu().numpy().copy()
+    # the table sits after the error word and the attention tickets (qsa.h, workspace size)
+    off = 256 + ((w.batch * w.kv_heads * 4 + 255) // 256) * 256
+    tab = db.ws[off:off + 16].cpu().numpy().view(np.uint32)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tab[0] == 0x51534231 and tab[1] == sms and tab[2] > 0, tab
+    for _ in range(4):
+        db.ids.fill_(-1)
+        db.out.fill_(float("nan"))
+        db.decode()
+        assert db.check_errors() == (0, 0)
+        assert db.ids.cpu().numpy().tobytes() == ids.tobytes()
+        assert db.out.cpu().numpy().tobytes() == out.tobytes()
+    w_sm = db.ws[off + 16 + 4 * 256:off + 16 + 8 * 256].cpu().numpy().view(np.uint32)
+    assert (w_sm > 0).sum() == sms and w_sm.min(initial=1 << 30) >= 0
+    assert w_sm[w_sm > 0].min() >= 1024 and w_sm.max() <= 16384

@@ -40,6 +40,8 @@ Layout make_layout(const qsa_dims *d)
     off += kWsAlign;
     L.off_tickets = off;
     off = align_up(off + B * size_t(d->kv_heads) * 4, kWsAlign);
+    L.off_bal = off;
+    off = align_up(off + sizeof(ScoreBalance), kWsAlign);
     const size_t nparts = B * size_t(d->q_heads) * size_t(L.nparts);
     L.off_part_m = off;
     off = align_up(off + nparts * 4, kWsAlign);
@@ -135,7 +137,8 @@ qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int6
     if (sms <= 0) return QSA_ERR_CUDA;
     ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, stride,
                 d->batch, d->idx_heads, d->idx_dim, d->max_visible, err_word(ws, L),
-                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride, pooled, pool_offset};
+                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride, pooled, pool_offset,
+                (pooled == nullptr && !shared) ? ws_at<ScoreBalance>(ws, L.off_bal) : nullptr, 0};
     return from_cuda(shared ? launch_score_shared(a, sms, s) : launch_score(a, sms, s));
 }
 
@@ -143,12 +146,12 @@ qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int6
 // exactly these scores (only inside qsa_decode).
 qsa_status do_select(const qsa_dims *d, const int32_t *visible, const float *scores, int64_t stride,
                      int32_t *ids, int32_t *n_ids, void *ws, const Layout &L, cudaStream_t s, bool use_hint,
-                     bool pdl = false)
+                     bool pdl = false, bool balance = false)
 {
     if (d->batch == 0) return QSA_OK;
     SelectArgs a{visible, scores, stride, ids, n_ids, L.row_cap, d->budget_groups, d->max_visible,
                  d->batch, err_word(ws, L), use_hint ? ws_at<uint32_t>(ws, L.off_qmax) : nullptr,
-                 L.qmax_stride};
+                 L.qmax_stride, balance ? ws_at<ScoreBalance>(ws, L.off_bal) : nullptr};
     return from_cuda(launch_select(a, s, pdl));
 }
 
@@ -386,7 +389,9 @@ qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *
     // The three launches overlap their launch latency with the predecessor's
     // tail (programmatic dependent launch) unless timing marks separate them.
     const bool pdl = n_events == 0;
-    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s, true, pdl)) != QSA_OK)
+    // (after the raw scorer: one spare selection CTA updates its per-SM weights)
+    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s, true, pdl,
+                        pooled == nullptr && !shared)) != QSA_OK)
         return st;
     if (!mark(2)) return QSA_ERR_CUDA;
     // K/V rows go from the cache to shared memory and nowhere else: no scratch

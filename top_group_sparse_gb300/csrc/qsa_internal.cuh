@@ -21,6 +21,28 @@ constexpr int kAttendRowsPerPart = 256;  // emitted rows per attention CTA
 constexpr int kAttendParts =             // attention CTAs (and partials) per (query, KV head) at
     (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 9
 constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
+
+// The raw scorer's per-SM balance (in the workspace; all zero at first).
+// The SMs do not stream equally fast -- the spread is mostly a property of
+// each SM, stable from launch to launch -- so each scorer CTA, launched two
+// per SM by a cooperative launch, takes a share of the tiles sized by the
+// measured speed of the SM it runs on.  Each CTA records its time; one spare
+// CTA of the following selection turns the times into the weights of the
+// next launch.  The weights only move work between CTAs: the scores do not
+// depend on them.
+constexpr int kBalSlots = 256;                 // SM ids covered (larger ids: equal shares)
+constexpr uint32_t kBalMagic = 0x51534231u;    // the weights below are complete
+struct ScoreBalance {
+    uint32_t magic;                  // kBalMagic once the weights are filled in
+    uint32_t nsm;                    // SMs with a weight
+    uint32_t w_total;                // sum of the weights
+    uint32_t pad;
+    uint32_t w_before[kBalSlots];    // sum of the weights of the lower SM ids
+    uint32_t w[kBalSlots];           // weight of each SM id (0: none)
+    uint32_t ctr[kBalSlots];         // CTAs ever started on the SM: tells its two CTAs apart
+    uint32_t el_ns[kBalSlots][2];    // the last cooperative launch: each CTA's time (ns) ...
+    uint32_t tiles[kBalSlots][2];    // ... and its tile count
+};
 constexpr size_t kWsAlign = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -49,7 +71,7 @@ struct Layout {
     int64_t qmax_stride;    // entries per row of quad maxima (selection hint)
     int32_t row_cap;        // IDs per row: 4*budget + 3
     int32_t nparts;         // attention partials per (query, head): kAttendParts
-    size_t off_err, off_tickets, off_part_m, off_part_l, off_part_acc;
+    size_t off_err, off_tickets, off_bal, off_part_m, off_part_l, off_part_acc;
     size_t off_qmax, off_scores;
     size_t total;
 };
@@ -74,6 +96,9 @@ struct ScoreArgs {
     // at row pool_offset[b] + g (idx_keys, key_offset unused)
     const float *pooled;
     const int64_t *pool_offset;
+    // raw keys only: the per-SM balance (nullptr: equal shares per CTA)
+    ScoreBalance *bal;
+    int32_t bal_coop;        // set by the launcher: a cooperative launch, two CTAs on every SM
 };
 bool score_shape_supported(int idx_heads, int idx_dim);
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
@@ -104,6 +129,9 @@ struct SelectArgs {
     uint32_t *err;
     const uint32_t *qmax;    // hint only: quad maxima as written by the scorer (may be stale)
     int64_t qmax_stride;
+    // non-null: one CTA more than the batch turns the scorer's recorded
+    // times into its next per-SM weights, once the scorer has finished
+    ScoreBalance *bal;
 };
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s, bool pdl = false);
 

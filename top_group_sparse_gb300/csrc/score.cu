@@ -111,6 +111,34 @@ __device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int end, int
     return end;
 }
 
+// The tile range of a CTA of a cooperative raw-key launch (kCtas per SM on
+// every SM): the share of this SM, by its weight, halved between its CTAs,
+// which tell themselves apart by a counter.  Without complete weights (the
+// first launch, another GPU size) the equal range passed in stays.  Writes
+// begin, end and the slot the CTA records its time in (-1: none).
+template <int kCtas>
+__device__ void balanced_range(ScoreBalance *bl, int total, int begin, int end, int *out)
+{
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    int slot = -1;
+    if (smid < uint32_t(kBalSlots)) {
+        const uint32_t magic = __ldcg(&bl->magic), nsm = __ldcg(&bl->nsm), wt = __ldcg(&bl->w_total);
+        const uint32_t wb = __ldcg(&bl->w_before[smid]), ws = __ldcg(&bl->w[smid]);
+        const uint32_t sub = atomicAdd(&bl->ctr[smid], 1u) % uint32_t(kCtas);
+        slot = int(smid) * 2 + int(sub);
+        if (magic == kBalMagic && nsm * kCtas == gridDim.x && ws > 0 && wt > 0 && wb + ws <= wt) {
+            const uint64_t den = uint64_t(kCtas) * wt;
+            const uint64_t u0 = uint64_t(kCtas) * wb + uint64_t(sub) * ws;
+            end = int(min(uint64_t(total), (uint64_t(total) * (u0 + ws)) / den));
+            begin = int(min(uint64_t(end), (uint64_t(total) * u0) / den));
+        }
+    }
+    out[0] = begin;
+    out[1] = end;
+    out[2] = slot;
+}
+
 template <int H, int D, bool kPooled>
 __global__ void __launch_bounds__(ScoreCfg<H, D, kPooled>::kThreads, ScoreCfg<H, D, kPooled>::kCtasPerSm)
 score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
@@ -130,8 +158,13 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     // Each CTA walks one contiguous range of tiles: it meets at most a couple
     // of queries (few reloads of q) and streams its keys sequentially.
     const int total = a.batch * tiles_per_q;
-    const int t_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
-    const int t_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
+    int t_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
+    int t_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
+    // a cooperative raw-key launch: the range comes from the per-SM weights
+    constexpr bool kBal = !kPooled && C::kCtasPerSm <= 2;
+    const bool bal = kBal && a.bal_coop != 0;
+    __shared__ int s_bal[3];
+    const uint64_t t_start = global_timer_ns();
 
     allow_successor_launch();  // selection CTAs fill SMs as this grid's CTAs retire
     if (blockIdx.x == 0) {
@@ -143,8 +176,13 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        if (bal) balanced_range<C::kCtasPerSm>(a.bal, total, t_begin, t_end, s_bal);
     }
     __syncthreads();
+    if (bal) {
+        t_begin = s_bal[0];
+        t_end = s_bal[1];
+    }
 
     // Producer state lives in thread 0: the next tile to issue.
     int t_issue = t_begin;
@@ -281,6 +319,11 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         ++it;
     }
 
+    if (bal && tid == 0 && s_bal[2] >= 0) {  // this CTA's time, for the next launch's weights
+        const uint64_t dt = global_timer_ns() - t_start;
+        a.bal->el_ns[s_bal[2] >> 1][s_bal[2] & 1] = uint32_t(dt < 0xffffffffull ? dt : 0xffffffffull);
+        a.bal->tiles[s_bal[2] >> 1][s_bal[2] & 1] = uint32_t(t_end - t_begin);
+    }
     if (timed_out && tid == 0) {
         set_error(a.err, QSA_DEVERR_WAIT_TIMEOUT);
         // Let every copy still in flight land (bounded) before the CTA exits.
@@ -313,7 +356,25 @@ cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
     }
     const long long slots = (long long)num_sms * resident[dev];
     const int grid = int(total < slots ? total : slots);
-    score_groups_kernel<H, D, kPooled><<<grid, C::kThreads, C::kSmem, s>>>(a, tiles_per_q);
+    ScoreArgs ab = a;
+    ab.bal_coop = 0;
+    if (!kPooled && C::kCtasPerSm <= 2 && a.bal != nullptr && grid == slots) {
+        // every SM gets exactly its resident CTAs: a cooperative launch (all
+        // CTAs resident at once), so ranges by SM cover the tiles exactly
+        ab.bal_coop = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(grid));
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, score_groups_kernel<H, D, kPooled>, ab, tiles_per_q);
+    }
+    score_groups_kernel<H, D, kPooled><<<grid, C::kThreads, C::kSmem, s>>>(ab, tiles_per_q);
     return cudaGetLastError();
 }
 

@@ -276,6 +276,58 @@ __device__ __forceinline__ void emit_in_order(KeyAt key_at, GroupAt group_at, in
     }
 }
 
+// The raw scorer's per-SM weights for its next launch, from the times its
+// CTAs recorded (run by one spare CTA, after the scorer has finished).  The
+// rate of an SM is its tiles over the time of its slower CTA; the weight is
+// that rate relative to the mean, x 4096, averaged with the weight the SM
+// had (the weights converge to the rates), kept within [1024, 16384].  The
+// recorded times are then cleared, so that a launch that records nothing
+// leaves the weights as they are.
+__device__ void balance_update(ScoreBalance *bl, SelSmem &sm)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool had = __ldcg(&bl->magic) == kBalMagic;
+    float rate = 0.0f;
+    uint32_t w_old = 0;
+    if (tid < kBalSlots) {
+        const uint32_t e0 = __ldcg(&bl->el_ns[tid][0]), e1 = __ldcg(&bl->el_ns[tid][1]);
+        const uint32_t t0 = __ldcg(&bl->tiles[tid][0]), t1 = __ldcg(&bl->tiles[tid][1]);
+        if (e0 > 0u) rate = float(t0 + t1) / float(max(e0, e1));
+        w_old = had ? __ldcg(&bl->w[tid]) : 0u;
+    }
+    float s = rate;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) sm.red[warp] = __float_as_uint(s);
+    const int n = __syncthreads_count(rate > 0.0f);
+    if (n == 0) return;  // nothing recorded since the last update
+    float total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) total += __uint_as_float(sm.red[w]);
+    const float mean = total / float(n);
+    uint32_t wn = 0;
+    if (rate > 0.0f && mean > 0.0f) {
+        const float r = rate / mean * 4096.0f;
+        const float u = w_old > 0u ? 0.5f * float(w_old) + 0.5f * r : r;
+        wn = uint32_t(fminf(fmaxf(u, 1024.0f), 16384.0f));
+    }
+    uint64_t tot;
+    const uint64_t before = block_excl_scan(wn, sm, &tot);
+    if (tid < kBalSlots) {
+        bl->w[tid] = wn;
+        bl->w_before[tid] = uint32_t(before);
+        bl->el_ns[tid][0] = 0u;
+        bl->el_ns[tid][1] = 0u;
+        bl->tiles[tid][0] = 0u;
+        bl->tiles[tid][1] = 0u;
+    }
+    if (tid == 0) {
+        bl->w_total = uint32_t(tot);
+        bl->nsm = uint32_t(n);
+        bl->magic = kBalMagic;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 select_emit_kernel(const SelectArgs a)
 {
@@ -283,6 +335,12 @@ select_emit_kernel(const SelectArgs a)
     SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    if (a.bal != nullptr && b == a.batch) {  // the spare CTA: the scorer's next weights
+        allow_successor_launch();
+        wait_for_predecessor();
+        balance_update(a.bal, sm);
+        return;
+    }
     allow_successor_launch();
     wait_for_predecessor();  // the scores (and quad maxima) come from the previous kernel;
                              // this kernel may start before that one ends, so what it wrote is
@@ -546,7 +604,8 @@ cudaError_t launch_select(const SelectArgs &a, cudaStream_t s, bool pdl)
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    return launch_kernel(select_emit_kernel, dim3(unsigned(a.batch)), dim3(kThreads), smem, s, pdl, a);
+    const unsigned grid = unsigned(a.batch) + (a.bal != nullptr ? 1u : 0u);
+    return launch_kernel(select_emit_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, a);
 }
 
 }  // namespace qsa
