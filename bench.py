@@ -421,27 +421,15 @@ def run_gpu(args):
 
     # ---- end to end through qsa_decode with host buffers -----------------------
     K2 = max(1, min(K, args.e2e_steps))
-    h_qidx = torch.from_numpy(w.q_idx).pin_memory()
-    h_q = torch.from_numpy(w.q).pin_memory()
-    h_vis = torch.from_numpy(w.visible).pin_memory()
-    h_koff = torch.from_numpy(w.key_offset).pin_memory()
-    h_soff = torch.from_numpy(w.slot_offset).pin_memory()
-    h_out = torch.empty(db.out.shape, dtype=torch.float32).pin_memory()
-    h_ids = torch.empty(db.ids.shape, dtype=torch.int32).pin_memory()
-    h_n = torch.empty(db.n_ids.shape, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_qidx, h_q, h_vis, h_koff, h_soff))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_ids, h_n))
+    # the step's own inputs (indexer queries, attention queries, visible
+    # lengths, history offsets) in one pinned buffer, its ID rows, counts and
+    # outputs in another: one copy each way per step
+    h_in, h_out = db.step_host_buffers()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        db.q_idx.copy_(h_qidx, non_blocking=True)
-        db.q.copy_(h_q, non_blocking=True)
-        db.visible.copy_(h_vis, non_blocking=True)
-        db.key_offset.copy_(h_koff, non_blocking=True)
-        db.slot_offset.copy_(h_soff, non_blocking=True)
-        db.decode(stream)
-        h_out.copy_(db.out, non_blocking=True)
-        h_ids.copy_(db.ids, non_blocking=True)
-        h_n.copy_(db.n_ids, non_blocking=True)
+        db.decode_from_host(h_in, h_out, stream)
         stream.synchronize()
 
     for _ in range(3):
@@ -502,9 +490,10 @@ def run_gpu(args):
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "note": "qsa_decode per step; queries copied in from pinned host memory, ID rows "
-                        "and outputs copied back, stream synchronised; K/V cache and index-key "
-                        "history resident in HBM"},
+                "note": "qsa_decode per step (DeviceBatch.decode_from_host); the step's queries, "
+                        "visible lengths and history offsets copied in from one pinned host buffer, "
+                        "ID rows, counts and outputs copied back into another, stream synchronised; "
+                        "K/V cache and index-key history resident in HBM"},
         "gpu_launches": 3 * K,
         "roofline": {"kernel": "score_groups", "bound": "hbm", "achieved": score_gbs,
                      "peak": peak, "unit": "GB/s", "frac": score_gbs / peak,

@@ -264,3 +264,26 @@ def test_per_sm_balance_engages_and_leaves_results_unchanged():
     w_sm = db.ws[off + 16 + 4 * 256:off + 16 + 8 * 256].cpu().numpy().view(np.uint32)
     assert (w_sm > 0).sum() == sms and w_sm.min(initial=1 << 30) >= 0
     assert w_sm[w_sm > 0].min() >= 1024 and w_sm.max() <= 16384
+
+
+def test_decode_from_host_buffers():
+    """One copy in, qsa_decode, one copy out: the host buffers carry exactly
+    the step's inputs and the device-side results."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    w = wl.make_workload("host", [9001, 37, 2052, 0], idx_heads=8, idx_dim=64, q_heads=16,
+                         kv_heads=2, head_dim=128, seed=91, slots="paged16")
+    db = qsa.DeviceBatch(w)
+    db.decode()
+    torch.cuda.synchronize()
+    ids, n, out = db.ids.cpu().numpy().copy(), db.n_ids.cpu().numpy().copy(), db.out.cpu().numpy().copy()
+    h_in, h_out = db.step_host_buffers()
+    db.ids.fill_(-1)
+    db.out.fill_(float("nan"))
+    db.q_idx.zero_()  # overwritten by the step's copy in
+    db.decode_from_host(h_in, h_out)
+    torch.cuda.synchronize()
+    hi, hn, ho = db.host_outputs(h_out)
+    assert hn.numpy().tobytes() == n.tobytes()
+    assert hi.numpy().tobytes() == ids.tobytes()
+    assert ho.numpy().tobytes() == out.tobytes()

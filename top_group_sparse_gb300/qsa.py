@@ -337,9 +337,45 @@ def qsa_attend_noalloc(dims, q, k_scr, v_scr, n_ids, out, stream=None) -> int:
 
 # ---- device-resident batch (plumbing: torch owns the memory) ----------------
 
+def _packed(arrays, device):
+    """One uint8 device buffer holding the given (name, numpy array or
+    (shape, dtype, fill)) items back to back, each on a 16-byte boundary;
+    returns (buffer, {name: typed view})."""
+    import torch
+    items, off = [], 0
+    for name, a in arrays:
+        if isinstance(a, tuple):
+            shape, dtype, fill = a
+            nbytes = int(np.prod(shape)) * np.dtype(dtype).itemsize
+        else:
+            a = np.ascontiguousarray(a)
+            shape, dtype, fill, nbytes = a.shape, a.dtype, None, a.nbytes
+        off = (off + 15) // 16 * 16
+        items.append((name, off, shape, dtype, fill, a))
+        off += nbytes
+    buf = torch.zeros(max(off, 16), dtype=torch.uint8, device=device)
+    views = {}
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32,
+           np.dtype(np.int64): torch.int64}
+    for name, o, shape, dtype, fill, a in items:
+        n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+        v = buf[o:o + n].view(tdt[np.dtype(dtype)]).view(tuple(shape))
+        if fill is None:
+            v.copy_(torch.from_numpy(a))
+        else:
+            v.fill_(fill)
+        views[name] = v
+    return buf, views
+
+
 class DeviceBatch:
     """The arrays of one workload copied into device memory, with the output
-    buffers and the workspace the library needs, all allocated by torch."""
+    buffers and the workspace the library needs, all allocated by torch.
+
+    A decode step's own inputs (q_idx, q, visible, key_offset, slot_offset)
+    share one buffer, `step_in`, and its outputs (ids, n_ids, out) another,
+    `step_out`: a step driven from host memory is one copy in and one copy
+    out (`step_host_buffers`, `decode_from_host`)."""
 
     def __init__(self, w, device="cuda", budget=None, queries=None):
         import torch
@@ -350,15 +386,15 @@ class DeviceBatch:
         def put(a):
             return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-        self.q_idx = put(w.q_idx[sel])
+        self.step_in, v = _packed([("q_idx", w.q_idx[sel]), ("q", w.q[sel]),
+                                   ("visible", w.visible[sel]), ("key_offset", w.key_offset[sel]),
+                                   ("slot_offset", w.slot_offset[sel])], dev)
+        self.q_idx, self.q, self.visible = v["q_idx"], v["q"], v["visible"]
+        self.key_offset, self.slot_offset = v["key_offset"], v["slot_offset"]
         self.idx_keys = put(w.idx_keys)
-        self.key_offset = put(w.key_offset[sel])
-        self.visible = put(w.visible[sel])
-        self.q = put(w.q[sel])
         self.k_cache = put(w.k_cache)
         self.v_cache = put(w.v_cache)
         self.slot_map = put(w.slot_map)
-        self.slot_offset = put(w.slot_offset[sel])
         B = len(sel)
         mv = int(w.visible[sel].max(initial=0))
         self.dims = make_dims(B, w.idx_heads, w.idx_dim, w.q_heads, w.kv_heads, w.head_dim,
@@ -376,12 +412,44 @@ class DeviceBatch:
             raise ValueError("invalid dims")
         # zero-filled: the workspace header must start clean
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-        self.ids = torch.full((B, self.row_cap), -1, dtype=torch.int32, device=dev)
-        self.n_ids = torch.full((B,), -1, dtype=torch.int32, device=dev)
-        self.out = torch.full((B, w.q_heads, w.head_dim), float("nan"), dtype=torch.float32, device=dev)
+        self.step_out, v = _packed([("ids", ((B, self.row_cap), np.int32, -1)),
+                                    ("n_ids", ((B,), np.int32, -1)),
+                                    ("out", ((B, w.q_heads, w.head_dim), np.float32, float("nan")))], dev)
+        self.ids, self.n_ids, self.out = v["ids"], v["n_ids"], v["out"]
         self.scores = torch.full((B, self.score_stride), float("nan"), dtype=torch.float32, device=dev)
         self.k_scr = torch.zeros((B, self.row_cap, w.kv_heads, w.head_dim), dtype=torch.float32, device=dev)
         self.v_scr = torch.zeros_like(self.k_scr)
+
+    # a decode step driven from host memory: one copy in, one copy out
+    def step_host_buffers(self):
+        """Pinned host buffers laid out like step_in (holding this batch's
+        current step inputs) and step_out."""
+        import torch
+        h_in = torch.empty(self.step_in.shape, dtype=torch.uint8).pin_memory()
+        h_in.copy_(self.step_in)
+        h_out = torch.empty(self.step_out.shape, dtype=torch.uint8).pin_memory()
+        return h_in, h_out
+
+    def decode_from_host(self, h_in, h_out, stream=None):
+        """One step on the current torch stream (or `stream`): the step's
+        inputs from h_in, qsa_decode, the ID rows, counts and outputs to
+        h_out (both copies asynchronous; synchronise before reading h_out)."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self.step_in.copy_(h_in, non_blocking=True)
+            self.decode(s)
+            h_out.copy_(self.step_out, non_blocking=True)
+
+    def host_outputs(self, h_out):
+        """(ids, n_ids, out) views of a host buffer laid out like step_out."""
+        import torch
+        res = []
+        for t in (self.ids, self.n_ids, self.out):
+            o = t.data_ptr() - self.step_out.data_ptr()
+            n = t.numel() * t.element_size()
+            res.append(h_out[o:o + n].view(t.dtype).view(t.shape))
+        return tuple(res)
 
     # the four stages and the whole path, on this batch's buffers
     def score(self, stream=None):
