@@ -434,6 +434,23 @@ def run_gpu(args):
 
     for _ in range(3):
         e2e_step()
+    # the step as one CUDA graph (copy in, three kernels, copy out), replayed
+    # each step; eager launches if this runtime cannot capture it
+    graph, e2e_mode = None, "eager"
+    try:
+        graph = db.capture_decode_from_host(h_in, h_out)
+        e2e_mode = "cuda_graph"
+    except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+        e2e_mode = f"eager (graph capture failed: {type(exc).__name__})"
+        torch.cuda.synchronize()
+    if graph is not None:
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                graph.replay()
+            stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
     barrier()
     t0 = time.perf_counter()
     for _ in range(K2):
@@ -490,6 +507,7 @@ def run_gpu(args):
                    "reasons": clocks["reasons"], "samples": clocks["samples"]},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
+                "launch": e2e_mode,
                 "note": "qsa_decode per step (DeviceBatch.decode_from_host); the step's queries, "
                         "visible lengths and history offsets copied in from one pinned host buffer, "
                         "ID rows, counts and outputs copied back into another, stream synchronised; "

@@ -287,3 +287,30 @@ def test_decode_from_host_buffers():
     assert hn.numpy().tobytes() == n.tobytes()
     assert hi.numpy().tobytes() == ids.tobytes()
     assert ho.numpy().tobytes() == out.tobytes()
+
+
+def test_decode_from_host_as_a_cuda_graph():
+    """The host-driven step captured once and replayed: same bits as eager,
+    and a replay after new inputs sees them."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    w = wl.long_262144(batch=2)
+    db = qsa.DeviceBatch(w)
+    h_in, h_out = db.step_host_buffers()
+    db.decode_from_host(h_in, h_out)
+    torch.cuda.synchronize()
+    ref = [t.numpy().copy() for t in db.host_outputs(h_out)]
+    g = db.capture_decode_from_host(h_in, h_out)
+    for _ in range(3):
+        h_out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.numpy() for t in db.host_outputs(h_out)]
+        assert all(a.tobytes() == b.tobytes() for a, b in zip(got, ref))
+    # new step inputs in the host buffer reach the replayed graph
+    qv = h_in[db.q.data_ptr() - db.step_in.data_ptr():][: db.q.numel() * 4].view(torch.float32)
+    qv.mul_(2.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert db.host_outputs(h_out)[2].numpy().tobytes() != ref[2].tobytes()
+    assert db.check_errors() == (0, 0)

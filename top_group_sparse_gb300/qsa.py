@@ -441,6 +441,23 @@ class DeviceBatch:
             self.decode(s)
             h_out.copy_(self.step_out, non_blocking=True)
 
+    def capture_decode_from_host(self, h_in, h_out):
+        """A CUDA graph of one host-driven step (copy in, qsa_decode, copy
+        out), for a loop that repeats it: `g.replay()` on the current stream
+        launches the whole step at once.  Run one eager step first (the
+        library's one-time per-device setup must not happen during capture).
+        The step reads the per-SM scorer weights from the workspace when it
+        runs, so replays keep learning them."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.decode_from_host(h_in, h_out, s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
     def host_outputs(self, h_out):
         """(ids, n_ids, out) views of a host buffer laid out like step_out."""
         import torch
