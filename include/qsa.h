@@ -127,7 +127,9 @@ typedef struct {
  *   B*score_stride*4 (scores) + B*qstride*4 (the largest score of
  *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
  *   to 32, G_max = max_visible/4) +
- *   B*n_q*9*(d+2)*4 (attention partials: 9 runs of 256 rows per head).
+ *   B*n_q*9*(d+2)*4 (attention partials: 9 runs of 256 rows per head) +
+ *   B*(4*budget+3)*4 + B*4 (qsa_decode's ID rows and counts, which its last
+ *   kernel then stores to the caller's ids / n_ids).
  * The compact K/V row of qsa_decode never reaches device memory, so the
  * workspace holds no K/V scratch. */
 size_t qsa_workspace_size(const qsa_dims *dims);
@@ -233,7 +235,11 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
  * written to device memory.  Outputs: ids, n_ids (as qsa_select) and out,
  * bit-identical to qsa_attend over qsa_gather's scratch.  The selection
  * launch has one spare CTA that turns the scorer's recorded times into its
- * per-SM shares for the next call on this workspace. */
+ * per-SM shares for the next call on this workspace.  The selection writes
+ * its rows to the workspace and the attention kernel, the last one of the
+ * call, stores them to ids / n_ids together with out: the three outputs may
+ * point to mapped (pinned) host memory, and then the results reach the host
+ * with no separate copy. */
 qsa_status qsa_decode(const qsa_dims *dims, const qsa_inputs *in, int32_t *ids,
                       int32_t *n_ids, float *out, void *ws, size_t ws_bytes, void *stream);
 

@@ -63,7 +63,7 @@ def test_workspace_formula(lib):
     nch = 9  # attention partials per head: runs of 256 rows over at most 2051 rows
     bal = 7424  # the scorer's per-SM balance table
     want = 256 + _align(B * nkv * 4) + bal + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
-        + _align(B * 16384 * 4) + _align(B * 65536 * 4)
+        + _align(B * 16384 * 4) + _align(B * 65536 * 4) + _align(B * 2051 * 4) + _align(B * 4)
     assert qsa.qsa_workspace_size(d) == want
     # doubling the history adds exactly the scores (and per-quad maxima) of the new groups
     a = qsa.qsa_workspace_size(_dims(max_visible=1 << 20))

@@ -290,8 +290,10 @@ def test_decode_from_host_buffers():
 
 
 def test_decode_from_host_as_a_cuda_graph():
-    """The host-driven step captured once and replayed: same bits as eager,
-    and a replay after new inputs sees them."""
+    """The host-driven step captured once and replayed, with the outputs
+    copied back and with the kernels storing them straight into the pinned
+    host buffer: same counts, rows (up to each count: entries past it are
+    untouched) and outputs as eager, and a replay after new inputs sees them."""
     torch = need_gpu()
     from top_group_sparse_gb300 import qsa
     w = wl.long_262144(batch=2)
@@ -300,13 +302,24 @@ def test_decode_from_host_as_a_cuda_graph():
     db.decode_from_host(h_in, h_out)
     torch.cuda.synchronize()
     ref = [t.numpy().copy() for t in db.host_outputs(h_out)]
-    g = db.capture_decode_from_host(h_in, h_out)
-    for _ in range(3):
-        h_out.zero_()
-        g.replay()
-        torch.cuda.synchronize()
-        got = [t.numpy() for t in db.host_outputs(h_out)]
-        assert all(a.tobytes() == b.tobytes() for a, b in zip(got, ref))
+
+    def same_as_ref():
+        ids, n, out = (t.numpy() for t in db.host_outputs(h_out))
+        if n.tobytes() != ref[1].tobytes() or out.tobytes() != ref[2].tobytes():
+            return False
+        return all(ids[b, :n[b]].tobytes() == ref[0][b, :n[b]].tobytes() for b in range(len(n)))
+
+    h_out.zero_()
+    db.decode_into_host(h_in, h_out)
+    torch.cuda.synchronize()
+    assert same_as_ref()
+    for direct in (False, True):
+        g = db.capture_decode_from_host(h_in, h_out, direct=direct)
+        for _ in range(3):
+            h_out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert same_as_ref(), direct
     # new step inputs in the host buffer reach the replayed graph
     qv = h_in[db.q.data_ptr() - db.step_in.data_ptr():][: db.q.numel() * 4].view(torch.float32)
     qv.mul_(2.0)

@@ -55,6 +55,10 @@ Layout make_layout(const qsa_dims *d)
     off = align_up(off + B * size_t(L.qmax_stride) * 4, kWsAlign);
     L.off_scores = off;
     off = align_up(off + B * size_t(L.score_stride) * 4, kWsAlign);
+    L.off_ids = off;   // the whole-path call's ID rows and counts, before the caller's copy
+    off = align_up(off + B * size_t(L.row_cap) * 4, kWsAlign);
+    L.off_nids = off;
+    off = align_up(off + B * 4, kWsAlign);
     L.total = off;
     return L;
 }
@@ -179,7 +183,7 @@ qsa_status do_attend(const qsa_dims *d, const float *q, const float *k_scr, cons
 
 qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
                             float *k_scr, float *v_scr, float *out, void *ws, const Layout &L, cudaStream_t s,
-                            bool pdl = false)
+                            bool pdl = false, int32_t *ids_out = nullptr, int32_t *n_ids_out = nullptr)
 {
     if (d->batch == 0) return QSA_OK;
     AttendArgs a{in->q, nullptr, nullptr, n_ids, out,
@@ -188,7 +192,7 @@ qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32
                  L.row_cap, L.nparts, d->batch, d->q_heads, d->kv_heads, d->head_dim,
                  d->scale, err_word(ws, L),
                  ids, in->visible, in->slot_map, in->slot_offset, in->k_cache, in->v_cache, in->num_slots,
-                 k_scr, v_scr};
+                 k_scr, v_scr, ids_out, n_ids_out};
     return from_cuda(launch_attend(a, s, pdl));
 }
 
@@ -390,12 +394,18 @@ qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *
     // tail (programmatic dependent launch) unless timing marks separate them.
     const bool pdl = n_events == 0;
     // (after the raw scorer: one spare selection CTA updates its per-SM weights)
-    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids, n_ids, ws, L, s, true, pdl,
+    // The rows go to the workspace; the attention kernel, which finishes the
+    // path, stores them with `out` to the caller's buffers (device or mapped
+    // host memory alike: no separate copy of the results).
+    int32_t *ids_ws = ws_at<int32_t>(ws, L.off_ids);
+    int32_t *n_ws = ws_at<int32_t>(ws, L.off_nids);
+    if ((st = do_select(dims, in->visible, scores, L.score_stride, ids_ws, n_ws, ws, L, s, true, pdl,
                         pooled == nullptr && !shared)) != QSA_OK)
         return st;
     if (!mark(2)) return QSA_ERR_CUDA;
     // K/V rows go from the cache to shared memory and nowhere else: no scratch
-    if ((st = do_gather_attend(dims, in, ids, n_ids, nullptr, nullptr, out, ws, L, s, pdl)) != QSA_OK) return st;
+    if ((st = do_gather_attend(dims, in, ids_ws, n_ws, nullptr, nullptr, out, ws, L, s, pdl, ids, n_ids)) != QSA_OK)
+        return st;
     if (!mark(3)) return QSA_ERR_CUDA;
     return QSA_OK;
 }

@@ -157,6 +157,10 @@ attend_kernel(const AttendArgs a)
     int id = 0;
     if (kFromCache && tid < kRowsPerPart && my_r < a.row_cap) id = __ldcg(a.ids + row_base + my_r);
     const int n = __ldcg(a.n_ids + b);
+    if (a.ids_out != nullptr && kvh == 0) {  // the caller's copy of the rows and the count
+        if (tid < kRowsPerPart && my_r < n && my_r < a.row_cap) a.ids_out[row_base + my_r] = id;
+        if (part == 0 && tid == 0) a.n_ids_out[b] = n;
+    }
     if (n < 0 || n > a.row_cap) {
         if (part == 0) {
             for (int e = tid; e < gq * D; e += kThreads) a.out[(int64_t(b) * a.q_heads + h0) * D + e] = 0.0f;

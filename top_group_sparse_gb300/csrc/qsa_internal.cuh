@@ -72,7 +72,7 @@ struct Layout {
     int32_t row_cap;        // IDs per row: 4*budget + 3
     int32_t nparts;         // attention partials per (query, head): kAttendParts
     size_t off_err, off_tickets, off_bal, off_part_m, off_part_l, off_part_acc;
-    size_t off_qmax, off_scores;
+    size_t off_qmax, off_scores, off_ids, off_nids;
     size_t total;
 };
 
@@ -169,6 +169,12 @@ struct AttendArgs {
     const float *k_cache, *v_cache;
     int64_t num_slots;
     float *k_scr_out, *v_scr_out;
+    // the whole-path call: ids / n_ids are the selection's rows in the
+    // workspace; each run CTA of KV head 0 also stores its rows (and CTA
+    // (run 0, KV head 0) the count) to the caller's ids_out / n_ids_out, as
+    // it stores `out` -- so the results reach the caller's memory, wherever it
+    // is, from the kernel that finishes the path (nullptr: not wanted)
+    int32_t *ids_out, *n_ids_out;
 };
 bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl = false);

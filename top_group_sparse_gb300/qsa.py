@@ -441,7 +441,20 @@ class DeviceBatch:
             self.decode(s)
             h_out.copy_(self.step_out, non_blocking=True)
 
-    def capture_decode_from_host(self, h_in, h_out):
+    def decode_into_host(self, h_in, h_out, stream=None):
+        """One step on the current torch stream (or `stream`): the step's
+        inputs copied in from h_in, then qsa_decode with its ID rows, counts
+        and outputs pointing straight into the pinned host buffer h_out (laid
+        out like step_out): the last kernel stores them there, so no copy
+        follows.  Synchronise before reading h_out."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        hi, hn, ho = self.host_outputs(h_out)
+        with torch.cuda.stream(s):
+            self.step_in.copy_(h_in, non_blocking=True)
+            qsa_decode(self.dims, self.inputs, hi, hn, ho, self.ws, s)
+
+    def capture_decode_from_host(self, h_in, h_out, direct=False):
         """A CUDA graph of one host-driven step (copy in, qsa_decode, copy
         out), for a loop that repeats it: `g.replay()` on the current stream
         launches the whole step at once.  Run one eager step first (the
@@ -454,7 +467,10 @@ class DeviceBatch:
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                self.decode_from_host(h_in, h_out, s)
+                if direct:
+                    self.decode_into_host(h_in, h_out, s)
+                else:
+                    self.decode_from_host(h_in, h_out, s)
         torch.cuda.current_stream().wait_stream(s)
         return g
 
