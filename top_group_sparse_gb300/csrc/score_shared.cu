@@ -15,13 +15,15 @@
 // qb) takes kQPC queries and one contiguous range of 32-group tiles.
 //
 // The FMA chains are cut into D/16 segments of 16 dims and run as a systolic
-// pipeline across the lanes of a warp: lane (seg, slot) holds q for 4 heads of
-// one query restricted to dims 16*seg .. 16*seg+15 (64 registers), applies each
-// pooled value it loads to all 4 heads, and hands its 4 running sums to the
-// lane of the next segment by a shuffle; at step t segment seg works on group
-// t - seg of the tile.  The chain order over j is unchanged -- the running sum
-// just moves between lanes -- and one 16-byte shared-memory load now feeds 16
-// FMAs instead of 4.
+// pipeline across the lanes of a warp: lane (seg, slot) holds q for all H
+// heads of one query restricted to dims 16*seg .. 16*seg+15 (16*H registers),
+// applies each pooled value it loads to every head, and hands its H running
+// sums to the lane of the next segment by a shuffle; at step t segment seg
+// works on group t - seg of the tile, and the last segment's lane finishes
+// the ordered head sum on its own.  The chain order over j is unchanged --
+// the running sum just moves between lanes -- and one 16-byte shared-memory
+// load feeds 4*H FMAs instead of 4.  (With H = 8 a CTA of 8 warps takes most
+// of an SM's registers: one CTA per SM.)
 #include "pooling.cuh"
 #include "qsa_internal.cuh"
 
@@ -34,7 +36,8 @@ struct SharedCfg {
     static constexpr int kWarps = kThreads / 32;
     static constexpr int kSeg = D / 16;               // chain segments of 16 dims
     static constexpr int kSlots = 32 / kSeg;          // lanes per segment
-    static constexpr int kHPS = 4;                    // heads held by a lane
+    static constexpr int kHPS = H;                    // heads held by a lane: all of them
+    static constexpr int kCtasPerSm = kHPS * 16 > 64 ? 1 : 2;  // q takes kHPS x 16 registers
     static constexpr int kSlotsPerQ = H / kHPS;       // lanes (per segment) of one query
     static constexpr int kQPW = kSlots / kSlotsPerQ;  // queries per warp
     static constexpr int kQPC = kQPW * kWarps;        // queries per CTA
@@ -44,12 +47,12 @@ struct SharedCfg {
     static constexpr int kPoolFloats = kTG * D;
     static constexpr size_t kSmem =
         size_t(kStages) * kStageBytes + 2 * size_t(kPoolFloats) * 4 + size_t(kStages) * 8;
-    static_assert(D % 16 == 0 && H % kHPS == 0 && kSlots % kSlotsPerQ == 0, "lane layout");
+    static_assert(D % 16 == 0 && kSlotsPerQ == 1, "lane layout: one lane per (segment, query)");
     static_assert(kTG % 4 == 0, "tiles hold whole quads of groups");
 };
 
 template <int H, int D>
-__global__ void __launch_bounds__(SharedCfg<H, D>::kThreads, 2)
+__global__ void __launch_bounds__(SharedCfg<H, D>::kThreads, SharedCfg<H, D>::kCtasPerSm)
 score_shared_kernel(const ScoreArgs a, const int n_ranges, const int tiles_total)
 {
     using C = SharedCfg<H, D>;
@@ -74,7 +77,7 @@ score_shared_kernel(const ScoreArgs a, const int n_ranges, const int tiles_total
         g_need = 0;
     }
     __syncthreads();
-    // this lane's query: its groups, the shared history check, q for 4 heads x 16 dims
+    // this lane's query: its groups, the shared history check, q for H heads x 16 dims
     int G = 0;
     if (have_q) {
         const int T = __ldg(a.visible + b);
@@ -128,7 +131,9 @@ score_shared_kernel(const ScoreArgs a, const int n_ranges, const int tiles_total
     if (tid == 0)
         for (int s = 0; s < C::kStages; ++s) issue(s);
 
-    float acc[C::kHPS] = {0.f, 0.f, 0.f, 0.f};
+    float acc[C::kHPS];
+#pragma unroll
+    for (int u = 0; u < C::kHPS; ++u) acc[u] = 0.0f;
     uint32_t qk = 0u;  // quad maximum under way (the writing lane)
     int it = 0;
     bool timed_out = false;
@@ -176,20 +181,11 @@ score_shared_kernel(const ScoreArgs a, const int n_ranges, const int tiles_total
             }
 #pragma unroll
             for (int u = 0; u < C::kHPS; ++u) acc[u] = a4[u];
-            // last segment: ReLU per head, head sum in order h = 0..H-1 across
-            // the kSlotsPerQ lanes of the query (every lane takes part)
+            // last segment: ReLU per head, head sum in order h = 0..H-1 (the
+            // lane holds every head of its query)
             float hs = 0.0f;
 #pragma unroll
             for (int u = 0; u < C::kHPS; ++u) hs = __fadd_rn(hs, a4[u] > 0.0f ? a4[u] : 0.0f);
-            if constexpr (C::kSlotsPerQ == 2) {
-                const float lower = __shfl_up_sync(0xffffffffu, hs, 1);  // heads 0..3 of the query
-                if (hq == 1) {
-                    float s2 = lower;
-#pragma unroll
-                    for (int u = 0; u < C::kHPS; ++u) s2 = __fadd_rn(s2, a4[u] > 0.0f ? a4[u] : 0.0f);
-                    hs = s2;
-                }
-            }
             const int gg = g0 + g;
             if (seg == C::kSeg - 1 && hq == C::kSlotsPerQ - 1 && g >= 0 && g < n && gg < G) {
                 a.scores[int64_t(b) * a.score_stride + gg] = hs;
@@ -225,7 +221,7 @@ cudaError_t launch_shared_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
     }
     const int qblocks = (a.batch + C::kQPC - 1) / C::kQPC;
     if (qblocks > 65535) return cudaErrorInvalidValue;
-    int ranges = (2 * num_sms) / qblocks;
+    int ranges = (C::kCtasPerSm * num_sms) / qblocks;
     if (ranges < 1) ranges = 1;
     if (ranges > tiles_total) ranges = tiles_total;
     score_shared_kernel<H, D><<<dim3(unsigned(ranges), unsigned(qblocks)), C::kThreads, C::kSmem, s>>>(
