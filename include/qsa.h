@@ -127,7 +127,7 @@ typedef struct {
  *   B*score_stride*4 (scores) + B*qstride*4 (the largest score of
  *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
  *   to 32, G_max = max_visible/4) +
- *   B*n_q*9*(d+2)*4 (attention partials: 9 runs of 256 rows per head) +
+ *   B*n_q*8*(d+2)*4 (attention partials: 8 runs of 264 rows per head) +
  *   B*(4*budget+3)*4 + B*4 (qsa_decode's ID rows and counts, which its last
  *   kernel then stores to the caller's ids / n_ids).
  * The compact K/V row of qsa_decode never reaches device memory, so the
@@ -207,7 +207,7 @@ qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t 
  * (KV head h / (n_q/n_kv)):
  *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
  * rows i < n_ids[b] visited in emitted order: the row is cut into runs of
- * 256 rows (9 at most), each run into steps of 8 consecutive rows dealt
+ * 264 rows (8 at most), each run into steps of 8 consecutive rows dealt
  * to 12 running states in turn; each state is a running
  * max / rescale / denominator / accumulator, and the states are merged in a
  * fixed order, then the runs in row order.  The split depends only on
@@ -330,10 +330,10 @@ qsa_status qsa_decode_shared(const qsa_dims *dims, const qsa_inputs *in, int32_t
  * runs.  Same arguments, kernel and results as qsa_attend, minus `ws`: the
  * error word, merge tickets and chunk partials live in one static device
  * array of QSA_ATTEND_NOALLOC_SCRATCH_BYTES.  Nothing is allocated or freed.
- *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*9*4)
- *    + align256(B*n_q*9*d*4) bytes must fit; larger dims return
+ *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*8*4)
+ *    + align256(B*n_q*8*d*4) bytes must fit; larger dims return
  *    QSA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (e.g. B=8,
- *    n_q=16, d=128 needs 0.6 MB: fits; B=64 at the same shape does not).
+ *    n_q=16, d=128 needs 0.5 MB: fits; B=64 at the same shape does not).
  *  - The first call on each device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and keeps it; make that
  *    first call before any stream capture.

@@ -60,7 +60,7 @@ def test_workspace_formula(lib):
     the compact K/V row of the whole-path call stays on chip, so no K/V scratch."""
     d = _dims()
     B, nq, nkv, hd = 8, 16, 2, 128
-    nch = 9  # attention partials per head: runs of 256 rows over at most 2051 rows
+    nch = 8  # attention partials per head: runs of 264 rows over at most 2051 rows
     bal = 7424  # the scorer's per-SM balance table
     want = 256 + _align(B * nkv * 4) + bal + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
         + _align(B * 16384 * 4) + _align(B * 65536 * 4) + _align(B * 2051 * 4) + _align(B * 4)

@@ -63,7 +63,7 @@ def test_attend_noalloc_matches_attend_on_two_calls_in_a_row():
 def test_attend_noalloc_rejects_dims_beyond_its_scratch():
     need_gpu()
     from top_group_sparse_gb300 import qsa
-    # 256 queries x 16 heads x 9 partials x 130 floats is ~19 MB > the fixed array
+    # 256 queries x 16 heads x 8 partials x 130 floats is ~17 MB > the fixed array
     dims = qsa.make_dims(256, 8, 64, 16, 2, 128, max_visible=100256)
     with pytest.raises(qsa.QsaError) as e:
         qsa.qsa_attend_noalloc(dims, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)

@@ -51,7 +51,7 @@ namespace qsa {
 namespace {
 
 constexpr int kRowsPerPart = kAttendRowsPerPart;
-constexpr int kParts = kAttendParts;               // 9 runs at most (2,051 rows)
+constexpr int kParts = kAttendParts;               // 8 runs at most (2,051 rows)
 constexpr int kStepRows = 8;                       // rows per warp step
 constexpr int kRing = 2;                           // steps in flight per warp (ring slots)
 constexpr int kWarps = 12;

@@ -17,9 +17,9 @@ namespace qsa {
 // ---- workspace layout -----------------------------------------------------
 
 constexpr int kGroup = 4;            // tokens per scored group
-constexpr int kAttendRowsPerPart = 256;  // emitted rows per attention CTA
+constexpr int kAttendRowsPerPart = 264;  // emitted rows per attention CTA (33 steps of 8)
 constexpr int kAttendParts =             // attention CTAs (and partials) per (query, KV head) at
-    (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 9
+    (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 8
 constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
 
 // The raw scorer's per-SM balance (in the workspace; all zero at first).
