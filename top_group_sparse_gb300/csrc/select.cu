@@ -279,8 +279,9 @@ __device__ __forceinline__ void emit_in_order(KeyAt key_at, GroupAt group_at, in
 // The raw scorer's per-SM weights for its next launch, from the times its
 // CTAs recorded (run by one spare CTA, after the scorer has finished).  The
 // rate of an SM is its tiles over the time of its slower CTA; the weight is
-// that rate relative to the mean, x 4096, averaged with the weight the SM
-// had (the weights converge to the rates), kept within [1024, 16384].  The
+// that rate relative to the mean, x 4096, folded into the weight the SM had
+// with a factor 1/4 (the weights converge to the rates without following
+// each launch's noise), kept within [1024, 16384].  The
 // recorded times are then cleared, so that a launch that records nothing
 // leaves the weights as they are.
 __device__ void balance_update(ScoreBalance *bl, SelSmem &sm)
@@ -308,7 +309,7 @@ __device__ void balance_update(ScoreBalance *bl, SelSmem &sm)
     uint32_t wn = 0;
     if (rate > 0.0f && mean > 0.0f) {
         const float r = rate / mean * 4096.0f;
-        const float u = w_old > 0u ? 0.5f * float(w_old) + 0.5f * r : r;
+        const float u = w_old > 0u ? 0.75f * float(w_old) + 0.25f * r : r;
         wn = uint32_t(fminf(fmaxf(u, 1024.0f), 16384.0f));
     }
     uint64_t tot;
