@@ -192,7 +192,7 @@ qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32
                  L.row_cap, L.nparts, d->batch, d->q_heads, d->kv_heads, d->head_dim,
                  d->scale, err_word(ws, L),
                  ids, in->visible, in->slot_map, in->slot_offset, in->k_cache, in->v_cache, in->num_slots,
-                 k_scr, v_scr, ids_out, n_ids_out};
+                 k_scr, v_scr, /*defer_merge (the launcher's)*/ 0, ids_out, n_ids_out};
     return from_cuda(launch_attend(a, s, pdl));
 }
 

@@ -18,9 +18,11 @@
 // rescale e^(m - m') of the denominator l and of the accumulator, then
 // l += sum_i e^(x_i - m') and acc += sum_i e^(x_i - m') v_i.  At the end of
 // the run the twelve warp states are merged in warp order (M = max m_w,
-// L = sum l_w e^(m_w - M), acc = sum acc_w e^(m_w - M)), and the last CTA of
-// the (query, KV head) to finish -- an atomic ticket, nothing waits --
-// merges the runs in order the same way and divides by L.  No floating-point
+// L = sum l_w e^(m_w - M), acc = sum acc_w e^(m_w - M)), and the runs are
+// merged in order the same way and divided by L (merge_runs): by the last CTA
+// of the (query, KV head) to finish -- an atomic ticket, nothing waits -- when
+// the grid is one wave, else by a second small launch after the grid, so that
+// no CTA holds its SM through the fence and the ticket.  No floating-point
 // atomics; the bits of a query's output do not depend on the rest of the batch.
 //
 // Data movement: the CTA's threads resolve every row of its run at once
@@ -107,6 +109,92 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[32], int lane)
             reduce_scatter<1, O / 2>(v, lane);
         }
     }
+}
+
+// The runs of (query b, KV head kvh) merged in run order from their states in
+// the workspace: M = max m_c, w_c = e^(m_c - M), L = sum_c l_c w_c,
+// out = (sum_c acc_c w_c) / L, c = 0..used-1 in order (0 for L = 0).  Every
+// thread of the CTA (kNT of them) calls it.
+template <int D, int GQ, int kNT>
+__device__ __forceinline__ void merge_runs(const AttendArgs &a, int b, int kvh, int used, float (&pw)[GQ][kParts],
+                                           float *l_fin)
+{
+    constexpr int F4 = D / 4;
+    const int tid = threadIdx.x;
+    const int gq = a.q_heads / a.kv_heads;
+    const int h0 = kvh * gq;
+    const int64_t hb0 = (int64_t(b) * a.q_heads + h0) * a.nparts;
+    // every load first (one round trip), then the weights, then the sums
+    const int e0 = tid;  // one (head, column) element per thread when gq * F4 <= kNT
+    const int hh0 = e0 / F4, jj0 = e0 - hh0 * F4;
+    float4 xv[kParts];
+    if (e0 < gq * F4) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh0) * a.nparts) * D) + jj0;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c)
+            xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < gq) {
+        const int64_t hb = hb0 + int64_t(tid) * a.nparts;
+        float pm[kParts], pl[kParts];
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) {
+            pm[c] = c < used ? __ldcg(a.part_m + hb + c) : -INFINITY;
+            pl[c] = c < used ? __ldcg(a.part_l + hb + c) : 0.0f;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) M = fmaxf(M, pm[c]);
+        float L = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) {
+            const float w = (c >= used || M == -INFINITY) ? 0.0f : expf(pm[c] - M);
+            if (c < used) L = fmaf(pl[c], w, L);
+            pw[tid][c] = w;
+        }
+        l_fin[tid] = L;
+    }
+    __syncthreads();
+    for (int e = tid; e < gq * F4; e += kNT) {
+        const int hh = e / F4, j4 = e - hh * F4;
+        if (e != e0) {  // more elements than threads: load this one now
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh) * a.nparts) * D) + j4;
+#pragma unroll
+            for (int c = 0; c < kParts; ++c)
+                xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kParts; ++c) {
+            if (c < used) {
+                const float w = pw[hh][c];
+                o.x = fmaf(xv[c].x, w, o.x);
+                o.y = fmaf(xv[c].y, w, o.y);
+                o.z = fmaf(xv[c].z, w, o.z);
+                o.w = fmaf(xv[c].w, w, o.w);
+            }
+        }
+        const float L = l_fin[hh];
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (L > 0.0f) r = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+        *reinterpret_cast<float4 *>(a.out + (int64_t(b) * a.q_heads + h0 + hh) * D + 4 * j4) = r;
+    }
+}
+
+constexpr int kMergeThreads = 256;
+
+// The second launch of a deferred merge: one CTA per (KV head, query).
+template <int D, int GQ>
+__global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const AttendArgs a)
+{
+    __shared__ float pw[GQ][kParts];
+    __shared__ float l_fin[GQ];
+    const int kvh = blockIdx.x, b = blockIdx.y;
+    wait_for_predecessor();  // the run states come from the attention launch
+    const int n = __ldcg(a.n_ids + b);
+    if (n < 0 || n > a.row_cap) return;  // the attention zeroed this output and flagged it
+    const int used = max(1, (n + kRowsPerPart - 1) / kRowsPerPart);
+    merge_runs<D, GQ, kMergeThreads>(a, b, kvh, used, pw, l_fin);
 }
 
 template <int D, int GQ, Src kSrc>
@@ -414,7 +502,8 @@ attend_kernel(const AttendArgs a)
         reinterpret_cast<float4 *>(a.part_acc + (pbase + int64_t(hh) * a.nparts) * D)[j4] = o;
     }
 
-    // ---- the last CTA of this (query, KV head) merges the runs in order ------------
+    // ---- the runs merged in order: by a second launch, or by the last CTA ---------
+    if (a.defer_merge) return;  // the kernel's end publishes the state to the merge launch
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -425,62 +514,7 @@ attend_kernel(const AttendArgs a)
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
-    const int64_t hb0 = (int64_t(b) * a.q_heads + h0) * a.nparts;
-    // every load first (one round trip), then the weights, then the sums
-    const int e0 = tid;  // one (head, column) element per thread when gq * F4 <= 256
-    const int hh0 = e0 / F4, jj0 = e0 - hh0 * F4;
-    float4 xv[kParts];
-    if (e0 < gq * F4) {
-        const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh0) * a.nparts) * D) + jj0;
-#pragma unroll
-        for (int c = 0; c < kParts; ++c)
-            xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (tid < gq) {
-        const int64_t hb = hb0 + int64_t(tid) * a.nparts;
-        float pm[kParts], pl[kParts];
-#pragma unroll
-        for (int c = 0; c < kParts; ++c) {
-            pm[c] = c < used ? __ldcg(a.part_m + hb + c) : -INFINITY;
-            pl[c] = c < used ? __ldcg(a.part_l + hb + c) : 0.0f;
-        }
-        float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kParts; ++c) M = fmaxf(M, pm[c]);
-        float L = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kParts; ++c) {
-            const float w = (c >= used || M == -INFINITY) ? 0.0f : expf(pm[c] - M);
-            if (c < used) L = fmaf(pl[c], w, L);
-            sm.pw[tid][c] = w;
-        }
-        sm.l_fin[tid] = L;
-    }
-    __syncthreads();
-    for (int e = tid; e < gq * F4; e += kThreads) {
-        const int hh = e / F4, j4 = e - hh * F4;
-        if (e != e0) {  // more elements than threads: load this one now
-            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + (hb0 + int64_t(hh) * a.nparts) * D) + j4;
-#pragma unroll
-            for (int c = 0; c < kParts; ++c)
-                xv[c] = c < used ? __ldcg(src + int64_t(c) * F4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < kParts; ++c) {
-            if (c < used) {
-                const float w = sm.pw[hh][c];
-                o.x = fmaf(xv[c].x, w, o.x);
-                o.y = fmaf(xv[c].y, w, o.y);
-                o.z = fmaf(xv[c].z, w, o.z);
-                o.w = fmaf(xv[c].w, w, o.w);
-            }
-        }
-        const float L = sm.l_fin[hh];
-        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (L > 0.0f) r = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
-        *reinterpret_cast<float4 *>(a.out + (int64_t(b) * a.q_heads + h0 + hh) * D + 4 * j4) = r;
-    }
+    merge_runs<D, GQ, kThreads>(a, b, kvh, used, sm.pw, sm.l_fin);
 }
 
 template <int D, int GQ, Src kSrc>
@@ -497,8 +531,23 @@ cudaError_t launch_attend_t(const AttendArgs &a, cudaStream_t s, bool pdl)
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    static int sms[64] = {};
+    if (sms[dev] == 0) {
+        int n = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        sms[dev] = n > 0 ? n : 1;
+    }
     const dim3 grid(kParts, unsigned(a.kv_heads), unsigned(a.batch));
-    return launch_kernel(attend_kernel<D, GQ, kSrc>, grid, dim3(kThreads), smem, s, pdl, a);
+    // One CTA fits an SM: in a grid of more than one wave every CTA would
+    // hold its SM through the merge's fence and ticket, so the runs' states
+    // are merged by a second launch instead (same arithmetic, same bits).
+    AttendArgs ad = a;
+    ad.defer_merge = (long long)kParts * a.kv_heads * a.batch > sms[dev] ? 1 : 0;
+    cudaError_t e = launch_kernel(attend_kernel<D, GQ, kSrc>, grid, dim3(kThreads), smem, s, pdl, ad);
+    if (e != cudaSuccess || !ad.defer_merge) return e;
+    return launch_kernel(attend_merge_kernel<D, GQ>, dim3(unsigned(a.kv_heads), unsigned(a.batch)),
+                         dim3(kMergeThreads), 0, s, true, ad);
 }
 
 template <int D, Src kSrc>

@@ -169,6 +169,10 @@ struct AttendArgs {
     const float *k_cache, *v_cache;
     int64_t num_slots;
     float *k_scr_out, *v_scr_out;
+    // set by the launcher (grids of more than one wave): every run CTA writes
+    // its state and leaves; a second, small launch merges the runs (the same
+    // arithmetic as the last CTA's merge, so the same bits)
+    int32_t defer_merge;
     // the whole-path call: ids / n_ids are the selection's rows in the
     // workspace; each run CTA of KV head 0 also stores its rows (and CTA
     // (run 0, KV head 0) the count) to the caller's ids_out / n_ids_out, as
