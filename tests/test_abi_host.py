@@ -142,3 +142,23 @@ def test_ffma_probe_rejects_bad_arguments(lib):
     for bps, iters in ((0, 10), (9, 10), (4, 0)):
         with pytest.raises(qsa.QsaError):
             qsa.qsa_probe_ffma(bps, iters, None, stream=0)
+
+
+def test_packed_step_buffers_layout():
+    """A decode step's inputs (and outputs) share one buffer: every item on a
+    16-byte boundary, typed views over its own bytes only, fills applied."""
+    import numpy as np
+    a = np.arange(6, dtype=np.float32).reshape(2, 3)
+    b = np.array([5, -7, 9], dtype=np.int64)
+    buf, v = qsa._packed([("a", a), ("b", b), ("c", ((3, 2), np.int32, -1)),
+                          ("d", ((5,), np.float32, float("nan")))], "cpu")
+    base = buf.data_ptr()
+    for name in ("a", "b", "c", "d"):
+        assert (v[name].data_ptr() - base) % 16 == 0, name
+    assert v["a"].numpy().tobytes() == a.tobytes() and v["b"].numpy().tobytes() == b.tobytes()
+    assert (v["c"].numpy() == -1).all() and np.isnan(v["d"].numpy()).all()
+    # no overlap: writing one view leaves the others as they were
+    v["c"].fill_(3)
+    assert v["a"].numpy().tobytes() == a.tobytes() and v["b"].numpy().tobytes() == b.tobytes()
+    ends = sorted((t.data_ptr() - base, t.data_ptr() - base + t.numel() * t.element_size()) for t in v.values())
+    assert all(e0 <= s1 for (_, e0), (s1, _) in zip(ends, ends[1:])) and ends[-1][1] <= buf.numel()
