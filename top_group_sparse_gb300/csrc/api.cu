@@ -150,12 +150,13 @@ qsa_status do_score(const qsa_dims *d, const qsa_inputs *in, float *scores, int6
 // exactly these scores (only inside qsa_decode).
 qsa_status do_select(const qsa_dims *d, const int32_t *visible, const float *scores, int64_t stride,
                      int32_t *ids, int32_t *n_ids, void *ws, const Layout &L, cudaStream_t s, bool use_hint,
-                     bool pdl = false, bool balance = false)
+                     bool pdl = false, bool balance = false, const qsa_inputs *prefetch_for = nullptr)
 {
     if (d->batch == 0) return QSA_OK;
     SelectArgs a{visible, scores, stride, ids, n_ids, L.row_cap, d->budget_groups, d->max_visible,
                  d->batch, err_word(ws, L), use_hint ? ws_at<uint32_t>(ws, L.off_qmax) : nullptr,
-                 L.qmax_stride, balance ? ws_at<ScoreBalance>(ws, L.off_bal) : nullptr};
+                 L.qmax_stride, balance ? ws_at<ScoreBalance>(ws, L.off_bal) : nullptr,
+                 prefetch_for ? prefetch_for->slot_map : nullptr, prefetch_for ? prefetch_for->slot_offset : nullptr};
     return from_cuda(launch_select(a, s, pdl));
 }
 
@@ -399,8 +400,9 @@ qsa_status decode_impl(const qsa_dims *dims, const qsa_inputs *in, const float *
     // host memory alike: no separate copy of the results).
     int32_t *ids_ws = ws_at<int32_t>(ws, L.off_ids);
     int32_t *n_ws = ws_at<int32_t>(ws, L.off_nids);
+    // (the chosen groups' slot-map entries are prefetched into L2 for the attention)
     if ((st = do_select(dims, in->visible, scores, L.score_stride, ids_ws, n_ws, ws, L, s, true, pdl,
-                        pooled == nullptr && !shared)) != QSA_OK)
+                        pooled == nullptr && !shared, in)) != QSA_OK)
         return st;
     if (!mark(2)) return QSA_ERR_CUDA;
     // K/V rows go from the cache to shared memory and nowhere else: no scratch

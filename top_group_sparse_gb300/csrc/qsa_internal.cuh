@@ -132,6 +132,10 @@ struct SelectArgs {
     // non-null: one CTA more than the batch turns the scorer's recorded
     // times into its next per-SM weights, once the scorer has finished
     ScoreBalance *bal;
+    // non-null: the slot-map entries of the chosen groups are prefetched into
+    // L2 for the attention kernel that follows (slot_map[slot_offset[b] + t])
+    const int32_t *slot_map;
+    const int64_t *slot_offset;
 };
 cudaError_t launch_select(const SelectArgs &a, cudaStream_t s, bool pdl = false);
 
@@ -326,6 +330,13 @@ __device__ __forceinline__ void wait_for_predecessor()
 __device__ __forceinline__ void allow_successor_launch()
 {
     asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+// Asks L2 to fetch the 128-byte line holding p (no data returned, nothing
+// waits).  Only for addresses the caller's own loads will touch.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;     // 1 s for a copy to land

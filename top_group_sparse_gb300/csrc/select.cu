@@ -357,6 +357,7 @@ select_emit_kernel(const SelectArgs a)
         qv[j] = (qmg != nullptr && q < a.qmax_stride) ? __ldcg(qmg + q) : 0u;
     }
     const int T = __ldg(a.visible + b);
+    const int32_t *smap = a.slot_map != nullptr ? a.slot_map + __ldg(a.slot_offset + b) : nullptr;
     int32_t *row = a.ids + int64_t(b) * a.row_cap;
     if (T < 0 || T > a.max_visible) {
         if (tid == 0) {
@@ -509,12 +510,15 @@ select_emit_kernel(const SelectArgs a)
             } else {
                 kth_largest([&](int i) { return sm.cand_key[i]; }, n, uint32_t(k), L, hi, sm, thr, need);
             }
-            // membership bitmaps
+            // membership bitmaps; the slot-map line of every possible member
+            // (4g < T: inside the query's slot map) is asked of L2 for the
+            // attention, which resolves the emitted IDs through it
             for (int i = tid; i < n; i += kThreads) {
                 const uint32_t key = sm.cand_key[i];
                 const int g = sm.cand_g[i];
                 if (key > thr) atomicOr(&sm.map_gt[g >> 5], 1u << (g & 31));
                 else if (key == thr) atomicOr(&sm.map_eq[g >> 5], 1u << (g & 31));
+                if (smap != nullptr && key >= thr) prefetch_l2(smap + 4 * int64_t(g));
             }
             __syncthreads();
             // Word prefixes: thread t takes the words of groups 64t .. 64t+63;
