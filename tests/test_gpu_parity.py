@@ -266,6 +266,30 @@ def test_per_sm_balance_engages_and_leaves_results_unchanged():
     assert w_sm[w_sm > 0].min() >= 1024 and w_sm.max() <= 16384
 
 
+def test_per_sm_shares_cover_every_tile():
+    """Under learned per-SM shares the raw scorer still writes every group's
+    score exactly once: the scores of a call on a workspace whose weights are
+    in place, written into a NaN-filled buffer (no score of an earlier call
+    can stand in for a missed tile), equal the oracle's bit for bit."""
+    torch = need_gpu()
+    import oracle
+    from top_group_sparse_gb300 import qsa
+    w = wl.long_262144(batch=2, seed=12)
+    db = qsa.DeviceBatch(w)
+    for _ in range(3):
+        db.decode()
+    off = 256 + ((w.batch * w.kv_heads * 4 + 255) // 256) * 256
+    assert db.ws[off:off + 4].cpu().numpy().view(np.uint32)[0] == 0x51534231
+    db.scores.fill_(float("nan"))
+    db.score()
+    assert db.check_errors() == (0, 0)
+    got = db.scores.cpu().numpy()
+    for b in range(w.batch):
+        ko, T = int(w.key_offset[b]), int(w.visible[b])
+        ref = oracle.score_groups(w.q_idx[b], w.idx_keys[ko:ko + T], T)
+        assert got[b, :T // 4].tobytes() == ref.tobytes(), b
+
+
 def test_decode_from_host_buffers():
     """One copy in, qsa_decode, one copy out: the host buffers carry exactly
     the step's inputs and the device-side results."""
