@@ -227,6 +227,31 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
                              const int32_t *n_ids, float *k_scr, float *v_scr, float *out,
                              void *ws, size_t ws_bytes, void *stream);
 
+/* The attention of qsa_gather_attend (rows resolved through the slot map and
+ * copied from the cache, visited in the order of qsa_attend) with its
+ * online-softmax state as the result instead of the normalised output, so
+ * that consecutive slices of one emitted row, attended separately (e.g. on
+ * the ranks that hold those tokens), combine into the row's attention
+ * ([AFN-017] Floating point makes order observable: the slices are merged in
+ * row order, a fixed order).  For each query b and head h, over the rows
+ * ids[b*row_cap + i], i < n_ids[b] (row_cap = qsa_row_capacity(dims); token
+ * IDs below visible[b], resolved as slot_map[slot_offset[b] + id]), with
+ * s_i = scale * q[b][h] . k_i:
+ *   m[b*n_q + h]    = max_i s_i                           (-inf for no rows)
+ *   l[b*n_q + h]    = sum_i e^(s_i - m)                   (0 for no rows)
+ *   acc[b][h][0..d) = sum_i e^(s_i - m) v_i               (0 for no rows)
+ * each sum taken in qsa_attend's order, so acc / l is qsa_attend's output
+ * bit for bit.  Slices r = 0, 1, ... of one row combine, in that order, as
+ * M = max m_r, L = sum_r l_r e^(m_r - M), out = (sum_r acc_r e^(m_r - M)) / L.
+ * acc: [B, n_q, d] (16-byte aligned); m, l: [B, n_q]; all device memory,
+ * caller-owned.  A row whose ID is outside [0, visible[b]) or whose slot is
+ * outside [0, num_slots) is taken as a zero K/V row and flagged
+ * (QSA_DEVERR_ROW_RANGE / QSA_DEVERR_SLOT_RANGE), as in qsa_decode; a count
+ * outside [0, row_cap] gives the empty state and QSA_DEVERR_ROW_RANGE. */
+qsa_status qsa_attend_state(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids,
+                            const int32_t *n_ids, float *acc, float *m, float *l,
+                            void *ws, size_t ws_bytes, void *stream);
+
 /* The whole path on `stream`: qsa_score_groups, qsa_select, then the
  * gather fused into the attention ([AFN-016] Why compact gather comes before
  * fusion: fusion once the compact path is measured, keeping logical IDs and

@@ -20,10 +20,10 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 21
+    assert len(names) == 22
     for n in names:
         assert hasattr(lib, n), n
-    for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",
+    for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_attend_state",
               "qsa_decode"):
         assert n in names
 
@@ -133,6 +133,14 @@ def test_validation_rejects_before_launch(lib):
     assert _raw("qsa_select", D(d), fake, fake + 4, fake, fake, fake, ws_need, None) == INVALID
     assert _raw("qsa_gather", D(d), I(inp), fake, fake, fake, fake + 4, fake, ws_need, None) == INVALID
     assert _raw("qsa_attend", D(d), fake, fake, fake, fake, fake, fake, 100, None) == WS_SMALL
+    # qsa_attend_state(dims, in, ids, n_ids, acc, m, l, ws, ws_bytes, stream)
+    st = "qsa_attend_state"
+    assert _raw(st, D(d), I(inp), fake, fake, fake, fake, None, fake, ws_need, None) == INVALID
+    assert _raw(st, D(d), I(inp), fake, fake, fake + 4, fake, fake, fake, ws_need, None) == INVALID
+    no_q = qsa.QsaInputs(fake, fake, fake, fake, None, fake, fake, 100, fake, fake)
+    assert _raw(st, D(d), I(no_q), fake, fake, fake, fake, fake, fake, ws_need, None) == INVALID
+    assert _raw(st, D(d), I(inp), fake, fake, fake, fake, fake, fake, ws_need - 1, None) == WS_SMALL
+    assert _raw(st, D(bad), I(inp), fake, fake, fake, fake, fake, fake, ws_need, None) == INVALID
     assert _raw("qsa_workspace_init", None, 10, None) == INVALID
     assert _raw("qsa_check_errors", fake, 8, None, None) == INVALID
 

@@ -184,7 +184,8 @@ qsa_status do_attend(const qsa_dims *d, const float *q, const float *k_scr, cons
 
 qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
                             float *k_scr, float *v_scr, float *out, void *ws, const Layout &L, cudaStream_t s,
-                            bool pdl = false, int32_t *ids_out = nullptr, int32_t *n_ids_out = nullptr)
+                            bool pdl = false, int32_t *ids_out = nullptr, int32_t *n_ids_out = nullptr,
+                            float *m_out = nullptr, float *l_out = nullptr)
 {
     if (d->batch == 0) return QSA_OK;
     AttendArgs a{in->q, nullptr, nullptr, n_ids, out,
@@ -193,7 +194,7 @@ qsa_status do_gather_attend(const qsa_dims *d, const qsa_inputs *in, const int32
                  L.row_cap, L.nparts, d->batch, d->q_heads, d->kv_heads, d->head_dim,
                  d->scale, err_word(ws, L),
                  ids, in->visible, in->slot_map, in->slot_offset, in->k_cache, in->v_cache, in->num_slots,
-                 k_scr, v_scr, /*defer_merge (the launcher's)*/ 0, ids_out, n_ids_out};
+                 k_scr, v_scr, /*defer_merge (the launcher's)*/ 0, ids_out, n_ids_out, m_out, l_out};
     return from_cuda(launch_attend(a, s, pdl));
 }
 
@@ -358,6 +359,23 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
     if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
     const Layout L = make_layout(dims);
     return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+qsa_status qsa_attend_state(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
+                            float *acc, float *m, float *l, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, false, true)) != QSA_OK) return st;
+    if ((st = check_inputs_gather(in)) != QSA_OK) return st;
+    if (!in->q || !aligned(in->q, 16)) return QSA_ERR_INVALID_ARG;
+    if (!ids || !n_ids || !acc || !m || !l) return QSA_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(n_ids, 4) || !aligned(acc, 16) || !aligned(m, 4) || !aligned(l, 4))
+        return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    const Layout L = make_layout(dims);
+    return do_gather_attend(dims, in, ids, n_ids, nullptr, nullptr, acc, ws, L, static_cast<cudaStream_t>(stream),
+                            false, nullptr, nullptr, m, l);
 }
 
 }  // extern "C"

@@ -113,8 +113,9 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[32], int lane)
 
 // The runs of (query b, KV head kvh) merged in run order from their states in
 // the workspace: M = max m_c, w_c = e^(m_c - M), L = sum_c l_c w_c,
-// out = (sum_c acc_c w_c) / L, c = 0..used-1 in order (0 for L = 0).  Every
-// thread of the CTA (kNT of them) calls it.
+// out = (sum_c acc_c w_c) / L, c = 0..used-1 in order (0 for L = 0); with the
+// state export, out = sum_c acc_c w_c, m_out = M, l_out = L.  Every thread of
+// the CTA (kNT of them) calls it.
 template <int D, int GQ, int kNT>
 __device__ __forceinline__ void merge_runs(const AttendArgs &a, int b, int kvh, int used, float (&pw)[GQ][kParts],
                                            float *l_fin)
@@ -153,6 +154,10 @@ __device__ __forceinline__ void merge_runs(const AttendArgs &a, int b, int kvh, 
             pw[tid][c] = w;
         }
         l_fin[tid] = L;
+        if (a.m_out != nullptr) {
+            a.m_out[int64_t(b) * a.q_heads + h0 + tid] = M;
+            a.l_out[int64_t(b) * a.q_heads + h0 + tid] = L;
+        }
     }
     __syncthreads();
     for (int e = tid; e < gq * F4; e += kNT) {
@@ -176,7 +181,8 @@ __device__ __forceinline__ void merge_runs(const AttendArgs &a, int b, int kvh, 
         }
         const float L = l_fin[hh];
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (L > 0.0f) r = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+        if (a.m_out != nullptr) r = o;
+        else if (L > 0.0f) r = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
         *reinterpret_cast<float4 *>(a.out + (int64_t(b) * a.q_heads + h0 + hh) * D + 4 * j4) = r;
     }
 }
@@ -252,6 +258,10 @@ attend_kernel(const AttendArgs a)
     if (n < 0 || n > a.row_cap) {
         if (part == 0) {
             for (int e = tid; e < gq * D; e += kThreads) a.out[(int64_t(b) * a.q_heads + h0) * D + e] = 0.0f;
+            if (a.m_out != nullptr && tid < gq) {  // the empty state
+                a.m_out[int64_t(b) * a.q_heads + h0 + tid] = -INFINITY;
+                a.l_out[int64_t(b) * a.q_heads + h0 + tid] = 0.0f;
+            }
             if (kvh == 0 && tid == 0) set_error(a.err, QSA_DEVERR_ROW_RANGE);
         }
         return;

@@ -183,6 +183,10 @@ struct AttendArgs {
     // it stores `out` -- so the results reach the caller's memory, wherever it
     // is, from the kernel that finishes the path (nullptr: not wanted)
     int32_t *ids_out, *n_ids_out;
+    // the state export: when m_out != nullptr, `out` receives the unnormalised
+    // accumulator sum_i e^(s_i - m) v_i of each head, m_out the running max m
+    // and l_out the denominator sum_i e^(s_i - m), instead of the output
+    float *m_out, *l_out;
 };
 bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl = false);

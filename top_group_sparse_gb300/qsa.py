@@ -17,7 +17,7 @@ __all__ = [
     "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
     "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
-    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_decode",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_attend_state", "qsa_decode",
     "qsa_decode_profiled", "qsa_attend_noalloc", "qsa_pool_groups", "qsa_score_pooled",
     "qsa_decode_pooled", "qsa_score_groups_shared", "qsa_decode_shared", "qsa_probe_ffma",
     "make_dims",
@@ -112,6 +112,8 @@ def load(path: str | None = None):
     L.qsa_attend.restype = ctypes.c_int
     L.qsa_gather_attend.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_gather_attend.restype = ctypes.c_int
+    L.qsa_attend_state.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.qsa_attend_state.restype = ctypes.c_int
     L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode.restype = ctypes.c_int
     L.qsa_decode_profiled.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P,
@@ -258,6 +260,15 @@ def qsa_gather_attend(dims, inputs, ids, n_ids, k_scr, v_scr, out, ws, stream=No
     return _check("qsa_gather_attend", load().qsa_gather_attend(
         ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(k_scr), _ptr(v_scr),
         _ptr(out), p, n, _stream(stream)))
+
+
+def qsa_attend_state(dims, inputs, ids, n_ids, acc, m, l, ws, stream=None) -> int:
+    """Online-softmax state (acc [B, n_q, d], m [B, n_q], l [B, n_q]) of each
+    query's rows ids[b, :n_ids[b]], resolved through the slot map."""
+    p, n = _ws(ws)
+    return _check("qsa_attend_state", load().qsa_attend_state(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(acc), _ptr(m), _ptr(l),
+        p, n, _stream(stream)))
 
 
 def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:
