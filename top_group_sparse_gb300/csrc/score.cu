@@ -114,8 +114,12 @@ __device__ __forceinline__ int next_tile(const ScoreArgs &a, int t, int end, int
 // The tile range of a CTA of a cooperative raw-key launch (kCtas per SM on
 // every SM): the share of this SM, by its weight, halved between its CTAs,
 // which tell themselves apart by a counter.  Without complete weights (the
-// first launch, another GPU size) the equal range passed in stays.  Writes
-// begin, end and the slot the CTA records its time in (-1: none).
+// first launch, another GPU size) the equal range passed in stays.  The
+// shares cover the tiles exactly when a launch runs on the SMs whose times
+// were recorded -- every SM of the GPU, for a process that has the whole
+// device; a cooperative launch the runtime refuses as too large (part of the
+// GPU is not this process's) falls back to equal shares.  Writes begin, end
+// and the slot the CTA records its time in (-1: none).
 template <int kCtas>
 __device__ void balanced_range(ScoreBalance *bl, int total, int begin, int end, int *out)
 {
@@ -372,7 +376,11 @@ cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, score_groups_kernel<H, D, kPooled>, ab, tiles_per_q);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, score_groups_kernel<H, D, kPooled>, ab, tiles_per_q);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        // not every SM is ours (e.g. a partitioned GPU): equal shares, ordinary launch
+        (void)cudaGetLastError();
+        ab.bal_coop = 0;
     }
     score_groups_kernel<H, D, kPooled><<<grid, C::kThreads, C::kSmem, s>>>(ab, tiles_per_q);
     return cudaGetLastError();
