@@ -3,6 +3,7 @@ declares; its host-only logic (sizes, stats, validation) runs without a GPU.
 No call here reaches a CUDA kernel: every compute call below is rejected by
 host-side validation before anything is enqueued."""
 import ctypes
+import os
 
 import pytest
 
@@ -170,3 +171,51 @@ def test_packed_step_buffers_layout():
     assert v["a"].numpy().tobytes() == a.tobytes() and v["b"].numpy().tobytes() == b.tobytes()
     ends = sorted((t.data_ptr() - base, t.data_ptr() - base + t.numel() * t.element_size()) for t in v.values())
     assert all(e0 <= s1 for (_, e0), (s1, _) in zip(ends, ends[1:])) and ends[-1][1] <= buf.numel()
+
+
+_C_CLIENT = r"""
+#include <stdio.h>
+#include "qsa.h"
+
+int main(void)
+{
+    qsa_dims d = {8, 8, 64, 16, 2, 128, 4, 512, 262144, 0.088388347648f};
+    int32_t visible[8] = {262144, 262144, 262144, 262144, 262144, 262144, 262144, 262144};
+    qsa_stats st;
+    qsa_dims bad = d;
+    bad.group = 5;
+    if (qsa_get_stats(&d, visible, &st) != QSA_OK) return 2;
+    printf("%zu %lld %d %lld %lld %lld %zu %s\n", qsa_workspace_size(&d), (long long)qsa_score_stride(&d),
+           (int)qsa_row_capacity(&d), (long long)st.selected_tokens, (long long)st.raw_key_bytes,
+           (long long)st.dense_mask_bytes, qsa_workspace_size(&bad),
+           qsa_status_string(QSA_ERR_WORKSPACE_TOO_SMALL) != NULL ? "named" : "null");
+    return 0;
+}
+"""
+
+
+def test_plain_c_client_links_and_calls_the_abi(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program (no C++, no torch) includes
+    qsa.h, links libqsa.so and calls its host-only entry points; the answers
+    equal the binding's and the closed forms."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(_C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(qsa.library_path())
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(qsa.__file__))), "include")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src),
+                    "-o", str(exe), "-L", libdir, "-lqsa", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    d = _dims()
+    assert int(out[0]) == qsa.qsa_workspace_size(d)
+    assert int(out[1]) == qsa.qsa_score_stride(d) == 65536
+    assert int(out[2]) == qsa.qsa_row_capacity(d) == 2051
+    assert int(out[3]) == 8 * 2048                    # 512 groups x 4 tokens, no tail
+    assert int(out[4]) == 8 * 262144 * 64 * 4         # the raw keys the scorer streams
+    assert int(out[5]) == 0                           # no query-by-key mask
+    assert int(out[6]) == 0 and out[7] == "named"
