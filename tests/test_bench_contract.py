@@ -1,0 +1,51 @@
+"""The benchmark's reference arm (the CPU oracle, timed on the host cores)
+keeps the one-line JSON contract, and its launch rules hold, on the CPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args, env=None, timeout=600):
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, env=e,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _bench("--impl", "reference", "--steps", "2", "--warmup", "3", "--batch", "1")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "queries/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "long_262144"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert abs(d["ms_per_step"] * d["value"] / 1e3 - 1.0) < 1e-6  # one query per step at batch 1
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _bench("--impl", "reference", "--steps", "2", "--warmup", "3",
+               env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("impl", ["reference", "gb300"])
+def test_fewer_than_three_warmup_steps_are_refused(impl):
+    r = _bench("--impl", impl, "--steps", "2", "--warmup", "2", timeout=120)
+    assert r.returncode != 0 and "warmup" in (r.stderr + r.stdout)
