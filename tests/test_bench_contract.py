@@ -49,3 +49,31 @@ def test_reference_arm_other_ranks_exit_without_work():
 def test_fewer_than_three_warmup_steps_are_refused(impl):
     r = _bench("--impl", impl, "--steps", "2", "--warmup", "2", timeout=120)
     assert r.returncode != 0 and "warmup" in (r.stderr + r.stdout)
+
+
+@pytest.mark.gpu
+def test_gpu_arm_prints_the_full_json_line():
+    """One short run of the benchmark's own arm: every key of the line, the
+    roofline of the scorer, the host-buffer end-to-end figure, the clock
+    record, the launch count (3 per step) and the parity sample."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    r = _bench("--steps", "5", "--warmup", "3", "--e2e-steps", "3", "--no-chunked", timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.strip()][-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "clocks", "e2e", "gpu_launches",
+                "roofline", "cpu_baseline"):
+        assert key in d, key
+    assert d["unit"] == "queries/s" and d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 5
+    assert d["config"]["workload"] == "long_262144" and "l2" in d["config"]
+    assert d["gpu_launches"] == 3 * 5
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9 and 0 < rf["frac"] < 1.5
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    assert d["parity_sample"]["ids_bit_exact"] is True
