@@ -22,8 +22,11 @@
 // merged in order the same way and divided by L (merge_runs): by the last CTA
 // of the (query, KV head) to finish -- an atomic ticket, nothing waits -- when
 // the grid is one wave, else by a second small launch after the grid, so that
-// no CTA holds its SM through the fence and the ticket.  No floating-point
-// atomics; the bits of a query's output do not depend on the rest of the batch.
+// no CTA holds its SM through the fence and the ticket.  With the state
+// export (AttendArgs::m_out) the merge stores M, L and the undivided acc
+// instead, so that separately attended slices of one row combine in row
+// order.  No floating-point atomics; the bits of a query's output do not
+// depend on the rest of the batch.
 //
 // Data movement: the CTA's threads resolve every row of its run at once
 // (one row each: the ID load, then the slot-map load).  Each warp then
