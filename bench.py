@@ -235,7 +235,9 @@ def run_gpu(args):
     from top_group_sparse_gb300 import build, qsa
     from top_group_sparse_gb300 import workloads as wl
     from top_group_sparse_gb300.sharding import max_over_ranks
-    build.build()
+    if local == 0:  # one build per node: the ranks share the in-tree library
+        build.build()
+    barrier()
     qsa.load()
 
     w = wl.long_262144(seed=4 + 1000 * rank, batch=args.batch)
