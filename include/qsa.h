@@ -148,9 +148,11 @@ const char *qsa_status_string(qsa_status status);
 
 /* ---- workspace ---------------------------------------------------------- */
 
-/* Zeroes the workspace header (error word and attention tickets).  Call once
- * after allocating a workspace, before its first use; a zero-filled
- * allocation needs no call.  Afterwards every call leaves the header clean. */
+/* Zeroes the ws_bytes of the workspace, whose header holds the error word,
+ * the attention tickets and the scorer's per-SM weights.  Call once after
+ * allocating a workspace, before its first use; a zero-filled allocation
+ * needs no call.  Afterwards every call leaves the tickets clean, and the
+ * weights are learned from the scorer's own timings. */
 qsa_status qsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, then reads and clears the sticky device error word
