@@ -5,6 +5,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -36,6 +37,28 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert abs(d["ms_per_step"] * d["value"] / 1e3 - 1.0) < 1e-6  # one query per step at batch 1
+
+
+def test_algorithmic_bytes_closed_forms():
+    """The roofline's numerators for the benchmark workload, from the closed
+    forms: per query 67,108,864 B of raw keys + 4,194,304 of selected K/V
+    (2,048 rows x 2 heads x 128 x 4 B x 2) + 8,192 of slot entries + 2,048
+    of indexer query + 16,384 of query and output; the scorer reads the keys
+    and the indexer query and writes 65,536 scores."""
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    w = types.SimpleNamespace(batch=8, visible=np.full(8, 262144, np.int32), budget=512, idx_heads=8,
+                              idx_dim=64, q_heads=16, kv_heads=2, head_dim=128)
+    path, scorer = bench.algorithmic_bytes(w)
+    assert path == 8 * (67108864 + 4194304 + 8192 + 2048 + 16384) == 570638336
+    assert scorer == 8 * (67108864 + 2048 + 65536 * 4) == 538984448
+    # a ragged query: 3 tail tokens join the row, and the scores count complete groups only
+    w.batch, w.visible = 1, np.array([4 * 1000 + 3], np.int32)
+    path, scorer = bench.algorithmic_bytes(w)
+    W = 4 * 512 + 3
+    assert path == 4003 * 64 * 4 + W * 2 * 128 * 4 * 2 + W * 4 + 8 * 64 * 4 + 2 * 16 * 128 * 4
+    assert scorer == 4003 * 64 * 4 + 8 * 64 * 4 + 1000 * 4
 
 
 def test_reference_arm_other_ranks_exit_without_work():
