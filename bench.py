@@ -42,6 +42,8 @@ WORKLOAD = "long_262144"
 FLUSH_BYTES = 256 << 20
 PROFILE = os.path.join(ROOT, "profiles", "score_groups_long_262144.md")
 SCORE_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score.cu")
+ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_long_262144.md")
+ATTEND_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "attend.cu")
 
 
 def config_dict(w):
@@ -59,9 +61,10 @@ def config_dict(w):
 
 
 def algorithmic_bytes(w):
-    """Bytes the method must move per query (raw index keys, selected K and
-    V rows, their slot-map entries, indexer and attention queries, output),
-    and the scorer's own per-launch bytes (raw keys + indexer query + scores)."""
+    """Bytes the method must move per step: the whole path (raw index keys,
+    selected K and V rows, their slot-map entries, indexer and attention
+    queries, output) and the scorer's own share (raw keys + indexer query;
+    the scores it writes are an intermediate, as is any scratch)."""
     per_q, scorer = [], 0
     for b in range(w.batch):
         T = int(w.visible[b])
@@ -69,8 +72,27 @@ def algorithmic_bytes(w):
         Wb = 4 * min(G, w.budget) + T % 4
         per_q.append(T * w.idx_dim * 4 + Wb * w.kv_heads * w.head_dim * 4 * 2 + Wb * 4 +
                      w.idx_heads * w.idx_dim * 4 + 2 * w.q_heads * w.head_dim * 4)
-        scorer += T * w.idx_dim * 4 + w.idx_heads * w.idx_dim * 4 + G * 4
+        scorer += T * w.idx_dim * 4 + w.idx_heads * w.idx_dim * 4
     return sum(per_q), scorer
+
+
+def attend_bytes(w):
+    """Algorithmic bytes of the fused gather + attention launch: the selected
+    K and V rows and their slot-map entries, the attention queries and the
+    output."""
+    total = 0
+    for b in range(w.batch):
+        T = int(w.visible[b])
+        Wb = 4 * min(T // 4, w.budget) + T % 4
+        total += Wb * (w.kv_heads * w.head_dim * 4 * 2 + 4) + 2 * w.q_heads * w.head_dim * 4
+    return total
+
+
+def attend_fma(w):
+    """Multiply-adds of the attention: every selected row, every query head,
+    q.k and p.v over the head width."""
+    rows = sum(4 * min(int(T) // 4, w.budget) + int(T) % 4 for T in w.visible)
+    return rows * w.q_heads * w.head_dim * 2
 
 
 def measured_peaks():
@@ -104,17 +126,20 @@ def ffma_peak(stream):
                    "best of 5 launches"}
 
 
-def profile_traffic():
-    """Per-launch DRAM bytes of the scorer from the committed ncu summary, or
-    None if it is missing or was taken on a different scorer source."""
-    if not os.path.exists(PROFILE):
+def profile_traffic(profile=PROFILE, src=SCORE_SRC):
+    """Per-launch DRAM bytes of a kernel at the benchmark's batch from its
+    committed ncu summary (`traffic_bytes_per_launch`), or None if the summary
+    is missing or was taken on a different source of the kernel (its
+    `<file>_sha256` line)."""
+    if not os.path.exists(profile):
         return None
-    text = open(PROFILE).read()
+    text = open(profile).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    h = re.search(r"score_cu_sha256:\s*([0-9a-f]{64})", text)
+    key = os.path.basename(src).replace(".", "_") + "_sha256"
+    h = re.search(key + r":\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(SCORE_SRC, "rb").read()).hexdigest()
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     return int(m.group(1)) if cur == h.group(1) else None
 
 
@@ -217,6 +242,99 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
+class Timer:
+    """Device timing of one path on one stream: before each call L2 is
+    flushed (FLUSH_BYTES written, then FLUSH_BYTES read, outside the events),
+    then the call is bracketed by CUDA events recorded on that stream; the
+    events are created before timing and the launches queue behind a short
+    device-side sleep, so host launch overhead is not timed."""
+
+    def __init__(self, device, stream):
+        import torch
+        self.torch = torch
+        self.stream = stream
+        self.flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.zeros(1, dtype=torch.float32, device=device)
+
+    def flush(self):
+        self.flush_w.zero_()
+        self.torch.sum(self.flush_r, dim=0, out=self.sink[0])
+
+    def events(self, n, per):
+        torch = self.torch
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(per)] for _ in range(n)]
+        for ev in evs:
+            for e in ev:
+                e.record(self.stream)
+        torch.cuda.synchronize()
+        return evs
+
+    def warm(self, fn, n):
+        for _ in range(n):
+            self.flush()
+            fn(self.stream)
+        self.torch.cuda.synchronize()
+
+    def run(self, fn, n):
+        """Per-call device times (ms) of n calls of fn(stream)."""
+        evs = self.events(n, 2)
+        self.torch.cuda._sleep(20_000_000)  # let the launches queue ahead of the device
+        for ev in evs:
+            self.flush()
+            ev[0].record(self.stream)
+            fn(self.stream)
+            ev[1].record(self.stream)
+        self.torch.cuda.synchronize()
+        return np.array([e[0].elapsed_time(e[1]) for e in evs])
+
+    def stages(self, db, n):
+        """Per-launch times (ms: scorer, selection, gather + attention) of n
+        qsa_decode_profiled calls (events between the three launches; this
+        form gives up the overlap of launch latencies, so its sum is a little
+        above the plain step)."""
+        evs = self.events(n, 4)
+        self.torch.cuda._sleep(20_000_000)
+        for ev in evs:
+            self.flush()
+            db.decode_profiled(ev, self.stream)
+        self.torch.cuda.synchronize()
+        return np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])
+
+
+def hbm_roofline(kernel, nbytes, ms, peak, peak_src, traffic=None, note=""):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+            "frac": gbs / peak, "traffic": traffic, "us_per_launch": ms * 1e3, "bytes_per_launch": int(nbytes),
+            "note": (note + "; " if note else "") + f"peak = {peak_src} HBM copy bandwidth"}
+
+
+def time_oracle(w, queries, n_threads, min_thread_s=10.0, max_s=12.0):
+    """The CPU oracle, as it stands, on n_threads host threads over the given
+    queries: passes repeat until about min_thread_s of host-thread time (at
+    least 4 passes, at most ~max_s of wall time)."""
+    import oracle
+    n = oracle.threads(n_threads)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode(w, queries=queries)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= 4 and (el * n >= min_thread_s or el >= max_s):
+            break
+    dt = time.perf_counter() - t0
+    return {"value": reps * len(queries) / dt, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{reps} pass(es) over {len(queries)} of the {w.batch} queries of the {w.name} "
+                      f"workload, plain C oracle on {n} host thread(s), {dt:.1f} s"}
+
+
+def oracle_pair(w, queries):
+    """The oracle on every host core (OpenMP over queries, groups and heads:
+    results identical to one thread) and on one thread."""
+    return time_oracle(w, queries, os.cpu_count() or 1), time_oracle(w, queries, 1)
+
+
 def run_gpu(args):
     import torch
     ws, rank, local = dist_env()
@@ -243,6 +361,10 @@ def run_gpu(args):
     w = wl.long_262144(seed=4 + 1000 * rank, batch=args.batch)
     db = qsa.DeviceBatch(w, device=f"cuda:{local}")
     stream = torch.cuda.current_stream()
+    dev = db.out.device
+    tm = Timer(dev, stream)
+    peak, peak_src = measured_peaks()
+    solo = ws == 1 and not args.no_cpu_baseline  # the oracle timings run at N=1 only
 
     # quick parity sample before timing: query 0's row against the oracle
     db.decode()
@@ -261,68 +383,27 @@ def run_gpu(args):
         if not ids_ok or err > 1e-5:
             raise SystemExit(f"parity check failed: {parity}")
 
-    flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=db.out.device)
-    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=db.out.device)
-    sink = torch.zeros(1, dtype=torch.float32, device=db.out.device)
+    def step(s):  # one qsa_decode call: the whole path over the batch
+        db.decode(s)
 
-    def flush():
-        flush_w.zero_()
-        torch.sum(flush_r, dim=0, out=sink[0])
-
-    def step(ev=None):
-        # one qsa_decode call; ev (two events) brackets it
-        if ev is not None:
-            ev[0].record(stream)
-        db.decode(stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize()
-
+    tm.warm(step, args.warmup)
     K = args.steps
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    for ev in events:  # create the CUDA events before the timed region
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
-        torch.cuda._sleep(20_000_000)  # let the launches queue ahead of the device
-        for k in range(K):
-            flush()
-            step(events[k])
-        torch.cuda.synchronize()
+        step_ms = tm.run(step, K)
         barrier()
         loop_wall = time.perf_counter() - t0
     st, flags = db.check_errors()
     if st != 0:
         raise SystemExit(f"device error word {flags:#x} after the timed loop")
-
-    step_ms = np.array([e[0].elapsed_time(e[1]) for e in events])
-    total_ms = max_over_ranks(float(step_ms.sum()), db.out.device)
-
-    # ---- per-kernel durations: the same steps through qsa_decode_profiled -------
-    # (events between its three launches; this form gives up the overlap of
-    # launch latencies, so its sum is a little above the plain step)
-    K3 = max(1, min(K, 500))
-    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K3)]
-    for ev in pev:
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
-    torch.cuda._sleep(20_000_000)
-    for k3 in range(K3):
-        flush()
-        db.decode_profiled(pev[k3], stream)
-    torch.cuda.synchronize()
-    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in pev])
+    total_ms = max_over_ranks(float(step_ms.sum()), dev)
     ms_per_step = total_ms / K
     value = ws * w.batch * K / (total_ms / 1e3)
+
+    # per-kernel durations: the same steps through qsa_decode_profiled
+    stage_mean = tm.stages(db, max(1, min(K, 500))).mean(axis=0)
 
     # ---- the incremental form: the scorer reads a pooled-key cache -------------
     # A decode step of this form appends the group its new token completes (one
@@ -331,95 +412,21 @@ def run_gpu(args):
     db.make_pooled_cache()
     db.pool_all()
     G_all = (w.visible // 4).astype(np.int32)
-    gb_t = torch.from_numpy(np.maximum(G_all - 1, 0)).to(db.out.device)
-    ge_t = torch.from_numpy(G_all).to(db.out.device)
+    gb_t = torch.from_numpy(np.maximum(G_all - 1, 0)).to(dev)
+    ge_t = torch.from_numpy(G_all).to(dev)
 
-    def inc_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        qsa.qsa_pool_groups(db.dims, db.inputs, gb_t, ge_t, 1, db.pooled, db.pool_offset, db.ws, stream)
-        db.decode_pooled(stream)
-        if ev is not None:
-            ev[1].record(stream)
+    def inc_step(s):
+        qsa.qsa_pool_groups(db.dims, db.inputs, gb_t, ge_t, 1, db.pooled, db.pool_offset, db.ws, s)
+        db.decode_pooled(s)
 
-    for _ in range(args.warmup):
-        flush()
-        inc_step()
-    torch.cuda.synchronize()
+    tm.warm(inc_step, args.warmup)
     K4 = max(1, min(K, 500))
-    iev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K4)]
-    for ev in iev:
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
-    torch.cuda._sleep(20_000_000)
-    for k4 in range(K4):
-        flush()
-        inc_step(iev[k4])
-    torch.cuda.synchronize()
+    inc_ms = max_over_ranks(float(tm.run(inc_step, K4).sum()), dev)
     st, flags = db.check_errors()
     if st != 0:
         raise SystemExit(f"device error word {flags:#x} in the incremental loop")
-    inc_ms = max_over_ranks(float(np.sum([e[0].elapsed_time(e[1]) for e in iev])), db.out.device)
     inc_value = ws * w.batch * K4 / (inc_ms / 1e3)
     del db.pooled
-
-    # ---- chunked prefill: 256 queries over one history, per-query vs shared ----
-    chunk = None
-    if not args.no_chunked:
-        wc = wl.chunked_prefill_100000()
-        dc = qsa.DeviceBatch(wc, device=f"cuda:{local}")
-
-        def time_path(fn, n=50):
-            for _ in range(3):
-                flush()
-                fn(stream)
-            torch.cuda.synchronize()
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-            for ev in evs:
-                for e in ev:
-                    e.record(stream)
-            torch.cuda.synchronize()
-            torch.cuda._sleep(20_000_000)
-            for ev in evs:
-                flush()
-                ev[0].record(stream)
-                fn(stream)
-                ev[1].record(stream)
-            torch.cuda.synchronize()
-            return float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-
-        ms_shared = time_path(dc.decode_shared)
-        ms_single = time_path(dc.decode)
-        ms_scorer = time_path(dc.score_shared)
-        st, flags = dc.check_errors()
-        if st != 0:
-            raise SystemExit(f"device error word {flags:#x} in the chunked-prefill loop")
-        # This workload is FFMA-bound (one key history, 256 queries): its
-        # roofline denominator is the FFMA rate measured here by the library's
-        # probe, beside the HBM one.
-        ffma = ffma_peak(stream)
-        Gs = wc.visible // 4
-        Ws = 4 * np.minimum(Gs, wc.budget) + wc.visible % 4
-        fma_score = int(np.sum(Gs.astype(np.int64)) * wc.idx_heads * wc.idx_dim)
-        fma_attend = int(np.sum(Ws.astype(np.int64)) * wc.q_heads * wc.head_dim * 2)
-        key_bytes = int(wc.visible.max()) * wc.idx_dim * 4  # the shared history, streamed once
-        chunk = {"workload": "chunked_prefill_100000", "queries_per_step": wc.batch,
-                 "shared": {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared},
-                 "per_query": {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single},
-                 "roofline": {"bound": "alu", "kernel": "score_shared_kernel (qsa_score_groups_shared)",
-                              "achieved": 2 * fma_score / (ms_scorer * 1e-3) / 1e12,
-                              "peak": ffma["tflops"], "unit": "TFLOP/s",
-                              "frac": 2 * fma_score / (ms_scorer * 1e-3) / 1e12 / ffma["tflops"],
-                              "us_per_launch": ms_scorer * 1e3, "fma_per_launch": fma_score,
-                              "peak_source": "measured in this run: " + ffma["how"],
-                              "hbm_frac": key_bytes / (ms_scorer * 1e-3) / 1e9 / measured_peaks()[0],
-                              "step_fma": fma_score + fma_attend,
-                              "step_frac": 2 * (fma_score + fma_attend) / (ms_shared * 1e-3) / 1e12 / ffma["tflops"]},
-                 "note": "256 queries at positions 100,000..100,255 of one history: qsa_decode_shared "
-                         "(each pooled tile scored for every query) vs qsa_decode (each query streams "
-                         "its own keys); outputs bit-identical (tests); L2 flushed before each step"}
-        del dc
 
     # ---- end to end through qsa_decode with host buffers -----------------------
     K2 = max(1, min(K, args.e2e_steps))
@@ -459,47 +466,123 @@ def run_gpu(args):
     t0 = time.perf_counter()
     for _ in range(K2):
         e2e_step()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, db.out.device)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     e2e_value = ws * w.batch * K2 / e2e_s
+
+    # ---- rooflines of the benchmark workload -------------------------------------
+    path_bytes, scorer_bytes = algorithmic_bytes(w)
+    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
+    G_q = int(w.visible[0]) // 4
+    inc_bytes = path_bytes - w.batch * (int(w.visible[0]) - G_q) * w.idx_dim * 4 + w.batch * 5 * w.idx_dim * 4
+    roof = hbm_roofline("score_groups", scorer_bytes, stage_mean[0], peak, peak_src,
+                        profile_traffic() if args.batch == 8 else None,
+                        f"algorithmic bytes {scorer_bytes} per launch (raw index keys + indexer queries; "
+                        "the scores written are an intermediate)")
+    roof_attend = hbm_roofline("attend_kernel (fused slot resolution, K/V gather and online softmax)",
+                               attend_bytes(w), stage_mean[2], peak, peak_src,
+                               profile_traffic(ATTEND_PROFILE, ATTEND_SRC) if args.batch == 8 else None,
+                               "selected K/V rows + slot entries + queries + outputs per launch; the time is "
+                               "the gather + attention stage of qsa_decode_profiled, its launch gap included")
+
+    # ---- the batched decode: 32 queries x 65,537 visible tokens ------------------
+    batched = None
+    if not args.no_batched:
+        w3 = wl.batched_65537()
+        d3 = qsa.DeviceBatch(w3, device=f"cuda:{local}")
+
+        def step3(s):
+            d3.decode(s)
+
+        tm.warm(step3, args.warmup)
+        K3 = max(1, min(K, 300))
+        ms3 = max_over_ranks(float(tm.run(step3, K3).sum()), dev) / K3
+        st3 = tm.stages(d3, max(1, min(K3, 200))).mean(axis=0)
+        st, flags = d3.check_errors()
+        if st != 0:
+            raise SystemExit(f"device error word {flags:#x} in the batched loop")
+        p3, s3 = algorithmic_bytes(w3)
+        batched = {
+            "workload": "batched_65537", "queries_per_step": w3.batch, "visible_tokens": int(w3.visible[0]),
+            "value": ws * w3.batch / (ms3 * 1e-3), "unit": UNIT, "ms_per_step": ms3, "steps": K3,
+            "roofline": hbm_roofline("score_groups", s3, st3[0], peak, peak_src, None,
+                                     f"algorithmic bytes {s3} per launch (raw index keys + indexer queries)"),
+            "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(w3), st3[2], peak, peak_src, None,
+                                            "selected K/V rows + slot entries + queries + outputs"),
+            "path_hbm": {"achieved_gbs": p3 / (ms3 * 1e-3) / 1e9, "frac_of_measured": p3 / (ms3 * 1e-3) / 1e9 / peak,
+                         "frac_of_8tbs": p3 / (ms3 * 1e-3) / 1e9 / 8000.0, "algorithmic_bytes_per_step": p3},
+            "stages_us": {n: float(v * 1e3) for n, v in zip(("score", "select", "gather_attend"), st3)},
+            "note": "32 independent histories of 65,537 tokens (16,384 groups + 1 tail token each), 16-token "
+                    "pages in a random permutation; one qsa_decode call per step, L2 flushed before each step"}
+        if solo and rank == 0:
+            batched["cpu_baseline"], batched["cpu_baseline_1thread"] = oracle_pair(w3, list(range(w3.batch)))
+        del d3, w3
+
+    # ---- chunked prefill: 256 queries over one history, shared vs per query -----
+    chunk = None
+    if not args.no_chunked:
+        wc = wl.chunked_prefill_100000()
+        dc = qsa.DeviceBatch(wc, device=f"cuda:{local}")
+
+        def time_path(fn, n=50):
+            tm.warm(fn, 3)
+            return float(tm.run(fn, n).mean())
+
+        ms_shared = time_path(dc.decode_shared)
+        ms_single = time_path(dc.decode)
+        ms_scorer_shared = time_path(dc.score_shared)
+        ms_scorer_single = time_path(dc.score)
+        stc = tm.stages(dc, 30).mean(axis=0)
+        st, flags = dc.check_errors()
+        if st != 0:
+            raise SystemExit(f"device error word {flags:#x} in the chunked-prefill loop")
+        # This workload is FFMA-bound (one key history, 256 queries): its
+        # roofline denominator is the FFMA rate measured here by the library's
+        # probe, beside the HBM one.
+        ffma = ffma_peak(stream)
+        Gs = wc.visible // 4
+        fma_score = int(np.sum(Gs.astype(np.int64)) * wc.idx_heads * wc.idx_dim)
+        fma_attend = attend_fma(wc)
+        key_bytes = int(wc.visible.max()) * wc.idx_dim * 4  # the shared history, streamed once
+
+        def alu_roofline(kernel, ms):
+            tf = 2 * fma_score / (ms * 1e-3) / 1e12
+            return {"kernel": kernel, "bound": "alu", "achieved": tf, "peak": ffma["tflops"], "unit": "TFLOP/s",
+                    "frac": tf / ffma["tflops"], "traffic": None, "us_per_launch": ms * 1e3,
+                    "fma_per_launch": fma_score, "peak_source": "measured in this run: " + ffma["how"],
+                    "hbm_frac": key_bytes / (ms * 1e-3) / 1e9 / peak}
+
+        cpu_c = None
+        if solo and rank == 0:
+            cpu_c = oracle_pair(wc, list(range(wc.batch)))
+        shared = {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared,
+                  "roofline": alu_roofline("score_shared_kernel (qsa_score_groups_shared)", ms_scorer_shared),
+                  "step_fma": fma_score + fma_attend,
+                  "step_frac": 2 * (fma_score + fma_attend) / (ms_shared * 1e-3) / 1e12 / ffma["tflops"]}
+        per_query = {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single,
+                     "roofline": alu_roofline("score_groups_kernel (qsa_score_groups; each query streams "
+                                              "its own keys, mostly from L2)", ms_scorer_single),
+                     "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(wc), stc[2], peak, peak_src,
+                                                     None, "selected K/V rows (many shared between queries, so "
+                                                     "read from L2) + slot entries + queries + outputs"),
+                     "stages_us": {n: float(v * 1e3) for n, v in zip(("score", "select", "gather_attend"), stc)}}
+        if cpu_c is not None:
+            for form in (shared, per_query):
+                form["cpu_baseline"], form["cpu_baseline_1thread"] = cpu_c
+        chunk = {"workload": "chunked_prefill_100000", "queries_per_step": wc.batch,
+                 "shared": shared, "per_query": per_query,
+                 "note": "256 queries at positions 100,000..100,255 of one history: qsa_decode_shared "
+                         "(each pooled tile scored for every query) vs qsa_decode (each query streams "
+                         "its own keys); outputs bit-identical (tests); L2 flushed before each step"}
+        del dc, wc
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
 
-    # ---- roofline of the dominant kernel (the scorer) --------------------------
-    path_bytes, scorer_bytes = algorithmic_bytes(w)
-    peak, peak_src = measured_peaks()
-    stage_mean = stage_ms.mean(axis=0)
-    score_gbs = scorer_bytes / (stage_mean[0] * 1e-3) / 1e9
-    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
-    G_q = int(w.visible[0]) // 4
-    inc_bytes = path_bytes - w.batch * (int(w.visible[0]) - G_q) * w.idx_dim * 4 + w.batch * 5 * w.idx_dim * 4
-
-    cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
-        import oracle
-        sample = list(range(w.batch))
-
-        def time_oracle(n_threads):
-            n = oracle.threads(n_threads)
-            t0 = time.perf_counter()
-            reps = 0
-            while True:  # about 10-16 s of host-thread time, at least 4 passes
-                oracle.decode(w, queries=sample)
-                reps += 1
-                el = time.perf_counter() - t0
-                if reps >= 4 and (el * n >= 10.0 or el >= 12.0):
-                    break
-            dt = time.perf_counter() - t0
-            return {"value": reps * len(sample) / dt, "unit": UNIT, "cores": n, "kind": "oracle",
-                    "sample": f"{reps} pass(es) over all {len(sample)} queries of the batch, plain C "
-                              f"oracle on {n} host thread(s), {dt:.1f} s"}
-
-        # every host core (OpenMP over queries, groups and heads: the same
-        # results as one thread), and one thread
-        cpu = time_oracle(os.cpu_count() or 1)
-        cpu_1t = time_oracle(1)
+    cpu = cpu_1t = None
+    if solo:
+        cpu, cpu_1t = oracle_pair(w, list(range(w.batch)))
 
     clocks = clk.summary()
     line = {
@@ -512,16 +595,13 @@ def run_gpu(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "launch": e2e_mode,
-                "note": "qsa_decode per step (DeviceBatch.decode_into_host); the step's queries, "
-                        "visible lengths and history offsets copied in from one pinned host buffer, "
-                        "ID rows, counts and outputs stored into another by the kernels, stream "
-                        "synchronised; K/V cache and index-key history resident in HBM"},
+                "note": "qsa_decode per step (DeviceBatch.decode_into_host); the step's queries, visible lengths "
+                        "and history offsets copied in from one pinned host buffer, ID rows, counts and outputs "
+                        "stored into another by the kernels, stream synchronised; K/V cache and index-key "
+                        "history resident in HBM"},
         "gpu_launches": 3 * K,
-        "roofline": {"kernel": "score_groups", "bound": "hbm", "achieved": score_gbs,
-                     "peak": peak, "unit": "GB/s", "frac": score_gbs / peak,
-                     "traffic": profile_traffic(),
-                     "note": f"algorithmic bytes {scorer_bytes} per launch (raw index keys + "
-                             f"indexer queries + scores), peak = {peak_src} HBM copy bandwidth"},
+        "roofline": roof,
+        "roofline_attend": roof_attend,
         "path_hbm": {"achieved_gbs": path_gbs, "frac_of_measured": path_gbs / peak,
                      "frac_of_8tbs": path_gbs / 8000.0, "algorithmic_bytes_per_step": path_bytes},
         "incremental": {"value": inc_value, "unit": UNIT, "ms_per_step": inc_ms / K4, "steps": K4,
@@ -530,9 +610,9 @@ def run_gpu(args):
                                 "(G*d_I*4 bytes per query instead of T*d_I*4): one qsa_pool_groups "
                                 "append of one group per query + qsa_decode_pooled per step; rows and "
                                 "outputs bit-identical to the full-raw path (tests)"},
+        "batched_65537": batched,
         "chunked_prefill": chunk,
-        "stages_us": {n: float(v * 1e3) for n, v in
-                      zip(("score", "select", "gather_attend"), stage_mean)},
+        "stages_us": {n: float(v * 1e3) for n, v in zip(("score", "select", "gather_attend"), stage_mean)},
         "loop_wall_s": loop_wall,
         "parity_sample": parity,
     }
@@ -557,6 +637,7 @@ def main():
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill side measurement")
+    ap.add_argument("--no-batched", action="store_true", help="skip the 32 x 65,537 batched-decode measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -108,13 +108,20 @@ typedef struct {
     int64_t candidate_groups;   /* sum_b floor(T_b/4)                            */
     int64_t selected_groups;    /* sum_b min(floor(T_b/4), budget)               */
     int64_t selected_tokens;    /* sum_b (4*selected groups + T_b mod 4)         */
-    int64_t raw_key_bytes;      /* index-key bytes the scorer reads              */
+    int64_t raw_key_bytes;      /* raw index-key bytes the scorer streams:       */
+                                /*   sum_b T_b*d_I*4 (full-raw form), 0 for the  */
+                                /*   incremental form, which reads pooled keys   */
     int64_t kv_bytes;           /* K and V bytes the gather reads                */
-    int64_t pooled_key_bytes;   /* pooled keys kept in device memory: 0 (they    */
-                                /*   live in shared memory only)                 */
+    int64_t pooled_key_bytes;   /* pooled keys held in device memory: 0 in the   */
+                                /*   full-raw form (its pooled tiles live in     */
+                                /*   shared memory only); the caller's pooled-   */
+                                /*   key cache in the incremental form           */
     int64_t workspace_bytes;    /* qsa_workspace_size(dims)                      */
     int64_t total_bytes;        /* raw_key + kv + pooled_key + workspace         */
-    int64_t dense_mask_bytes;   /* bytes of any query-by-key mask: always 0      */
+    int64_t dense_mask_bytes;   /* bytes of any query-by-key mask: 0 by          */
+                                /*   construction -- no entry point allocates or */
+                                /*   writes one, and the workspace formula below */
+                                /*   has no queries x keys term                  */
 } qsa_stats;
 
 /* ---- sizes (host only, no CUDA call) ---------------------------------- */
@@ -127,7 +134,7 @@ typedef struct {
  *   B*score_stride*4 (scores) + B*qstride*4 (the largest score of
  *   every four groups, a selection aid; qstride = ceil(G_max/4) rounded up
  *   to 32, G_max = max_visible/4) +
- *   B*n_q*8*(d+2)*4 (attention partials: 8 runs of 264 rows per head) +
+ *   B*n_q*17*(d+2)*4 (attention partials: 17 runs of 128 rows per head) +
  *   B*(4*budget+3)*4 + B*4 (qsa_decode's ID rows and counts, which its last
  *   kernel then stores to the caller's ids / n_ids).
  * The compact K/V row of qsa_decode never reaches device memory, so the
@@ -141,8 +148,18 @@ int64_t qsa_score_stride(const qsa_dims *dims);
  * [AFN-016] Decision). */
 int32_t qsa_row_capacity(const qsa_dims *dims);
 
-/* Fills *out from the dims and the host copy of visible ([B] T_b). */
+/* Fills *out for the full-raw form (qsa_decode) from the dims and the host
+ * copy of visible ([B] T_b). */
 qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_stats *out);
+
+/* Fills *out for the incremental form (qsa_decode_pooled): the scorer streams
+ * sum_b floor(T_b/4)*d_I*4 bytes of pooled keys instead of raw keys
+ * (raw_key_bytes = 0), and pooled_key_bytes counts the caller's pooled-key
+ * cache of pooled_rows rows of d_I floats (queries that share a history
+ * share its rows, so pooled_rows is the sum of floor(T/4) over the distinct
+ * histories when the cache holds exactly their complete groups). */
+qsa_status qsa_get_stats_pooled(const qsa_dims *dims, const int32_t *visible_host, int64_t pooled_rows,
+                                qsa_stats *out);
 
 const char *qsa_status_string(qsa_status status);
 
@@ -209,8 +226,8 @@ qsa_status qsa_gather(const qsa_dims *dims, const qsa_inputs *in, const int32_t 
  * (KV head h / (n_q/n_kv)):
  *   out[b][h] = sum_i softmax_i(scale * q[b][h] . k_scr[b][i]) v_scr[b][i],
  * rows i < n_ids[b] visited in emitted order: the row is cut into runs of
- * 264 rows (8 at most), each run into steps of 8 consecutive rows dealt
- * to 12 running states in turn; each state is a running
+ * 128 rows (17 at most), each run into steps of 4 consecutive rows dealt
+ * to 8 running states in turn; each state is a running
  * max / rescale / denominator / accumulator, and the states are merged in a
  * fixed order, then the runs in row order.  The split depends only on
  * n_ids[b], so results do not depend on the batch.  n_ids[b] = 0 gives a
@@ -253,6 +270,22 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
 qsa_status qsa_attend_state(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids,
                             const int32_t *n_ids, float *acc, float *m, float *l,
                             void *ws, size_t ws_bytes, void *stream);
+
+/* Joins the attention states of consecutive slices of one emitted row -- as
+ * qsa_attend_state returns them, e.g. one slice per rank holding those
+ * tokens -- into the row's output ([AFN-017] Floating point makes order
+ * observable: the slices merge in row order, a fixed order).  For each query
+ * b and head h, with slices r = 0 .. n_parts-1 in that order:
+ *   M = max_r m_r,  w_r = e^(m_r - M)  (0 when M = -inf),  L = sum_r l_r w_r,
+ *   out[b][h] = (sum_r acc_r w_r) / L   (0 when L = 0),
+ * both sums taken in slice order with the arithmetic the attention kernels
+ * use to merge their own runs, so one slice holding a whole row gives
+ * qsa_decode's output bit for bit.  m, l: [n_parts, B, n_q] (4-byte
+ * aligned); acc: [n_parts, B, n_q, d] and out: [B, n_q, d] (16-byte
+ * aligned); all device memory, caller-owned; n_parts >= 1.  Reads dims->
+ * batch, q_heads, kv_heads and head_dim; needs no workspace. */
+qsa_status qsa_merge_states(const qsa_dims *dims, int32_t n_parts, const float *m, const float *l,
+                            const float *acc, float *out, void *stream);
 
 /* The whole path on `stream`: qsa_score_groups, qsa_select, then the
  * gather fused into the attention ([AFN-016] Why compact gather comes before
@@ -357,13 +390,16 @@ qsa_status qsa_decode_shared(const qsa_dims *dims, const qsa_inputs *in, int32_t
  * runs.  Same arguments, kernel and results as qsa_attend, minus `ws`: the
  * error word, merge tickets and chunk partials live in one static device
  * array of QSA_ATTEND_NOALLOC_SCRATCH_BYTES.  Nothing is allocated or freed.
- *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*8*4)
- *    + align256(B*n_q*8*d*4) bytes must fit; larger dims return
+ *  - Size limit: 256 + align256(B*n_kv*4) + 2*align256(B*n_q*17*4)
+ *    + align256(B*n_q*17*d*4) bytes must fit; larger dims return
  *    QSA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (e.g. B=8,
- *    n_q=16, d=128 needs 0.5 MB: fits; B=64 at the same shape does not).
+ *    n_q=16, d=128 needs 1.1 MB: fits; B=32 at the same shape does not).
  *  - The first call on each device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress) and keeps it; make that
- *    first call before any stream capture.
+ *    array's device address (cudaGetSymbolAddress) and keeps it for the
+ *    life of the process; make that first call before any stream capture.
+ *    A cudaDeviceReset() can reload the library's device code at another
+ *    address, so do not use this call after resetting the device in the
+ *    same process.
  *  - Every call shares the array and it keeps the last call's contents: each
  *    call clears the error word and tickets on `stream` first.  Calls that
  *    overlap on the GPU (other streams, other threads) race on it.

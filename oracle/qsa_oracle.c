@@ -287,6 +287,37 @@ void qsao_attend_partial(const float *q, int32_t n_q, int32_t n_kv, int32_t d, f
     }
 }
 
+/* Online-softmax states of consecutive slices of one row merged in slice
+ * order -- the step that joins slices attended apart ("Top-k chooses the set;
+ * time chooses the order", Floating point makes order observable: the merge
+ * keeps the row's time order).  m, l: [n_parts, n_q]; acc: [n_parts, n_q, d].
+ * Starting from slice 0, slice r is folded in as one more block of the
+ * online softmax:
+ *   m' = max(m, m_r),  a = e^(m - m'),  a_r = e^(m_r - m')   (0 for m = -inf),
+ *   l  = l a + l_r a_r,  acc = acc a + acc_r a_r,  m = m'.
+ * out: [n_q, d] = acc / l (0 when l = 0). */
+void qsao_merge_states(int32_t n_parts, int32_t n_q, int32_t d, const float *m_in, const float *l_in,
+                       const float *acc_in, float *out)
+{
+    for (int32_t h = 0; h < n_q; ++h) {
+        float m = -INFINITY, l = 0.0f;
+        float *acc = out + (int64_t)h * d;
+        for (int32_t j = 0; j < d; ++j) acc[j] = 0.0f;
+        for (int32_t r = 0; r < n_parts; ++r) {
+            const float mr = m_in[(int64_t)r * n_q + h];
+            const float lr = l_in[(int64_t)r * n_q + h];
+            const float *ar = acc_in + ((int64_t)r * n_q + h) * d;
+            const float mn = mr > m ? mr : m;
+            const float a = (m == -INFINITY) ? 0.0f : expf(m - mn);
+            const float b = (mr == -INFINITY) ? 0.0f : expf(mr - mn);
+            l = l * a + lr * b;
+            for (int32_t j = 0; j < d; ++j) acc[j] = acc[j] * a + ar[j] * b;
+            m = mn;
+        }
+        for (int32_t j = 0; j < d; ++j) acc[j] = l > 0.0f ? acc[j] / l : 0.0f;
+    }
+}
+
 /* out: [n_q, d] = acc / l of the state above (0 for an empty row): the
  * attention of the q heads over the rows in the given order. */
 void qsao_attend(const float *q, int32_t n_q, int32_t n_kv, int32_t d, float scale,

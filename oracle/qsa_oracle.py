@@ -23,7 +23,7 @@ import numpy as np
 __all__ = [
     "build", "lib", "num_groups", "tail_len", "row_width", "pool_group",
     "score_groups", "score_groups_incremental", "pool_cache", "select", "dense_ids",
-    "resolve", "attend", "attend_partial", "decode", "threads", "GROUP",
+    "resolve", "attend", "attend_partial", "merge_states", "decode", "threads", "GROUP",
 ]
 
 GROUP = 4
@@ -125,6 +125,8 @@ def _declare(L):
     L.qsao_attend_partial.argtypes = [_F32P, _i32, _i32, _i32, _f32, _F32P, _F32P, _I32P, _i32,
                                       _F32P, _F32P, _F32P]
     L.qsao_attend_partial.restype = None
+    L.qsao_merge_states.argtypes = [_i32, _i32, _i32, _F32P, _F32P, _F32P, _F32P]
+    L.qsao_merge_states.restype = None
     L.qsao_decode.argtypes = [
         _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
         _F32P, _F32P, _I64P, _I32P, _F32P, _F32P, _F32P, _i64, _I32P, _I64P,
@@ -293,6 +295,21 @@ def attend_partial(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                               m.ctypes.data_as(_F32P), l.ctypes.data_as(_F32P),
                               acc.ctypes.data_as(_F32P))
     return m, l, acc
+
+
+def merge_states(parts):
+    """Output [n_q, d] of one row from the online-softmax states (m [n_q],
+    l [n_q], acc [n_q, d]) of its consecutive slices, given in row order:
+    each slice folded in as one more block of the online softmax."""
+    n = len(parts)
+    m = np.ascontiguousarray(np.stack([np.asarray(p[0], np.float32) for p in parts]))
+    l = np.ascontiguousarray(np.stack([np.asarray(p[1], np.float32) for p in parts]))
+    acc = np.ascontiguousarray(np.stack([np.asarray(p[2], np.float32) for p in parts]))
+    n_q, d = acc.shape[1], acc.shape[2]
+    out = np.empty((n_q, d), np.float32)
+    lib().qsao_merge_states(n, n_q, d, m.ctypes.data_as(_F32P), l.ctypes.data_as(_F32P),
+                            acc.ctypes.data_as(_F32P), out.ctypes.data_as(_F32P))
+    return out
 
 
 def decode(w, with_scores: bool = False, queries=None):

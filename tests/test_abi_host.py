@@ -21,12 +21,17 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = qsa.exported_symbols()
-    assert len(names) == 22
+    assert len(names) == 24
     for n in names:
         assert hasattr(lib, n), n
     for n in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_attend_state",
               "qsa_decode"):
         assert n in names
+    # the failure-detection self-test, declared apart from the hot path
+    selftest = qsa.exported_symbols(os.path.join(os.path.dirname(qsa.library_path()), "..", "..", "include",
+                                                 "qsa_selftest.h"))
+    assert selftest == ["qsa_selftest_copy_timeout"]
+    assert hasattr(lib, selftest[0])
 
 
 def test_status_strings(lib):
@@ -61,7 +66,7 @@ def test_workspace_formula(lib):
     the compact K/V row of the whole-path call stays on chip, so no K/V scratch."""
     d = _dims()
     B, nq, nkv, hd = 8, 16, 2, 128
-    nch = 8  # attention partials per head: runs of 264 rows over at most 2051 rows
+    nch = 17  # attention partials per head: runs of 128 rows over at most 2051 rows
     bal = 7424  # the scorer's per-SM balance table
     want = 256 + _align(B * nkv * 4) + bal + 2 * _align(B * nq * nch * 4) + _align(B * nq * nch * hd * 4) \
         + _align(B * 16384 * 4) + _align(B * 65536 * 4) + _align(B * 2051 * 4) + _align(B * 4)
@@ -103,6 +108,32 @@ def test_stats_closed_forms(lib):
         qsa.qsa_get_stats(d, [0, 1, 2, 300001])
 
 
+def test_stats_of_the_incremental_form(lib):
+    """Byte ownership of the incremental form ("A sparse mask is not sparse
+    attention", What the checkpoint measures: raw-key, K/V, pooled-key,
+    workspace and total bytes): the scorer streams no raw keys, and the
+    pooled-key cache -- floor(T/4) rows of d_I floats per history, shared by
+    the queries of one history -- is counted and included in the total."""
+    # three chunked-prefill queries over one history of 100,256 tokens, and a
+    # decode query with its own history of 262,144 tokens
+    d = _dims(batch=4, max_visible=300000)
+    vis = [100001, 100002, 100256, 262144]
+    histories = {0: 100256, 1: 262144}  # history -> tokens it holds
+    rows = sum(T // 4 for T in histories.values())
+    full = qsa.qsa_get_stats(d, vis)
+    st = qsa.qsa_get_stats_pooled(d, vis, rows)
+    assert st["pooled_key_bytes"] == (100256 // 4 + 262144 // 4) * 64 * 4
+    assert st["raw_key_bytes"] == 0
+    for key in ("candidate_groups", "selected_groups", "selected_tokens", "kv_bytes", "workspace_bytes"):
+        assert st[key] == full[key], key
+    assert st["total_bytes"] == st["kv_bytes"] + st["pooled_key_bytes"] + st["workspace_bytes"]
+    assert st["dense_mask_bytes"] == 0
+    # the cache holds 4x fewer bytes than the raw keys of the same histories
+    assert st["pooled_key_bytes"] * 4 == sum(histories.values()) * 64 * 4
+    with pytest.raises(qsa.QsaError):
+        qsa.qsa_get_stats_pooled(d, vis, -1)
+
+
 def _raw(fn, *args):
     return getattr(qsa.load(), fn)(*args)
 
@@ -142,6 +173,21 @@ def test_validation_rejects_before_launch(lib):
     assert _raw(st, D(d), I(no_q), fake, fake, fake, fake, fake, fake, ws_need, None) == INVALID
     assert _raw(st, D(d), I(inp), fake, fake, fake, fake, fake, fake, ws_need - 1, None) == WS_SMALL
     assert _raw(st, D(bad), I(inp), fake, fake, fake, fake, fake, fake, ws_need, None) == INVALID
+    # qsa_merge_states(dims, n_parts, m, l, acc, out, stream)
+    ms = "qsa_merge_states"
+    assert _raw(ms, D(d), 0, fake, fake, fake, fake, None) == INVALID
+    assert _raw(ms, D(d), 2, None, fake, fake, fake, None) == INVALID
+    assert _raw(ms, D(d), 2, fake, fake, fake + 4, fake, None) == INVALID
+    assert _raw(ms, D(d), 2, fake, fake, fake, fake + 8, None) == INVALID
+    assert _raw(ms, D(d), 2, fake + 2, fake, fake, fake, None) == INVALID
+    assert _raw(ms, D(bad), 2, fake, fake, fake, fake, None) == INVALID
+    assert _raw(ms, D(_dims(batch=2, max_visible=4096, head_dim=96)), 2, fake, fake, fake, fake, None) == UNSUPPORTED
+    # qsa_selftest_copy_timeout(dims, in, scores, ws, ws_bytes, wait_ns, stream)
+    tst = "qsa_selftest_copy_timeout"
+    assert _raw(tst, D(d), I(inp), fake, fake, ws_need, ctypes.c_uint64(0), None) == INVALID
+    assert _raw(tst, D(d), I(inp), fake, fake, ws_need, ctypes.c_uint64(2_000_000_000), None) == INVALID
+    assert _raw(tst, D(d), I(inp), fake, fake, ws_need - 1, ctypes.c_uint64(1000), None) == WS_SMALL
+    assert _raw(tst, D(d), I(null_inp), fake, fake, ws_need, ctypes.c_uint64(1000), None) == INVALID
     assert _raw("qsa_workspace_init", None, 10, None) == INVALID
     assert _raw("qsa_check_errors", fake, 8, None, None) == INVALID
 

@@ -44,7 +44,9 @@ def test_algorithmic_bytes_closed_forms():
     forms: per query 67,108,864 B of raw keys + 4,194,304 of selected K/V
     (2,048 rows x 2 heads x 128 x 4 B x 2) + 8,192 of slot entries + 2,048
     of indexer query + 16,384 of query and output; the scorer reads the keys
-    and the indexer query and writes 65,536 scores."""
+    and the indexer query (the scores it writes are an intermediate); the
+    fused gather + attention reads the selected K/V rows and their slot
+    entries and the query, and writes the output."""
     import types
     sys.path.insert(0, ROOT)
     import bench
@@ -52,13 +54,21 @@ def test_algorithmic_bytes_closed_forms():
                               idx_dim=64, q_heads=16, kv_heads=2, head_dim=128)
     path, scorer = bench.algorithmic_bytes(w)
     assert path == 8 * (67108864 + 4194304 + 8192 + 2048 + 16384) == 570638336
-    assert scorer == 8 * (67108864 + 2048 + 65536 * 4) == 538984448
+    assert scorer == 8 * (67108864 + 2048) == 536887296
+    assert bench.attend_bytes(w) == 8 * (4194304 + 8192 + 16384) == 33751040
+    assert bench.attend_fma(w) == 8 * 2048 * 16 * 128 * 2
+    # the batched workload: 65,537 tokens (16,384 groups and one tail token)
+    w3 = types.SimpleNamespace(batch=32, visible=np.full(32, 65537, np.int32), budget=512, idx_heads=8,
+                               idx_dim=64, q_heads=16, kv_heads=2, head_dim=128)
+    path3, scorer3 = bench.algorithmic_bytes(w3)
+    assert path3 == 32 * 21000452 == 672014464
+    assert scorer3 == 32 * (16777472 + 2048)
     # a ragged query: 3 tail tokens join the row, and the scores count complete groups only
     w.batch, w.visible = 1, np.array([4 * 1000 + 3], np.int32)
     path, scorer = bench.algorithmic_bytes(w)
     W = 4 * 512 + 3
     assert path == 4003 * 64 * 4 + W * 2 * 128 * 4 * 2 + W * 4 + 8 * 64 * 4 + 2 * 16 * 128 * 4
-    assert scorer == 4003 * 64 * 4 + 8 * 64 * 4 + 1000 * 4
+    assert scorer == 4003 * 64 * 4 + 8 * 64 * 4
 
 
 def test_reference_arm_other_ranks_exit_without_work():
@@ -100,3 +110,12 @@ def test_gpu_arm_prints_the_full_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert d["parity_sample"]["ids_bit_exact"] is True
+    ra = d["roofline_attend"]
+    assert ra["bound"] == "hbm" and ra["bytes_per_launch"] == 33751040
+    assert abs(ra["frac"] - ra["achieved"] / ra["peak"]) < 1e-9 and 0 < ra["frac"] < 1.5
+    b3 = d["batched_65537"]  # the 32 x 65,537 workload: its own sub-line
+    assert b3["value"] > 0 and b3["ms_per_step"] > 0 and b3["queries_per_step"] == 32
+    assert b3["path_hbm"]["algorithmic_bytes_per_step"] == 672014464
+    for rf in (b3["roofline"], b3["roofline_attend"]):
+        assert rf["bound"] == "hbm" and 0 < rf["frac"] < 1.5
+    assert b3["cpu_baseline"]["cores"] >= 1 and b3["cpu_baseline_1thread"]["cores"] == 1

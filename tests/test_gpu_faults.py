@@ -79,3 +79,46 @@ def test_workspace_init_and_clean_tickets():
     torch.cuda.synchronize()
     assert torch.equal(first, db.out)
     assert int(db.ws[:512].count_nonzero()) == 0  # error word and tickets
+
+
+def test_copy_wait_timeout_is_reported_and_the_workspace_stays_usable():
+    """Failure detection without a fault (the non-completion gate): the
+    scorer runs with its copy producer switched off (qsa_selftest_copy_timeout),
+    so every CTA's bounded wait runs out after 2 ms.  The error word reports
+    QSA_DEVERR_WAIT_TIMEOUT, no score is written, and the read clears the
+    word.  The same workspace then decodes exactly as one that never timed
+    out (rows, counts and outputs bit for bit), and under its learned per-SM
+    shares the scorer still writes every score, equal to the oracle's."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    from gpu_helpers import assert_scores_equal
+    w = wl.make_workload("timeout", [65537, 40003, 2052], idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2,
+                         head_dim=128, seed=61, slots="paged16")
+    db = qsa.DeviceBatch(w)
+    fresh = qsa.DeviceBatch(w)
+    for _ in range(3):  # both workspaces learn their per-SM scorer weights
+        db.decode()
+        fresh.decode()
+    assert db.check_errors() == (0, 0) and fresh.check_errors() == (0, 0)
+    db.scores.fill_(float("nan"))
+    qsa.qsa_selftest_copy_timeout(db.dims, db.inputs, db.scores, db.ws, 2_000_000)
+    st, flags = db.check_errors()
+    assert st == qsa.QSA_ERR_DEVICE_FAULT and flags == qsa.QSA_DEVERR_WAIT_TIMEOUT
+    assert bool(torch.isnan(db.scores).all())
+    assert db.check_errors() == (0, 0)  # read and cleared
+    for _ in range(3):
+        db.decode()
+        fresh.decode()
+        assert db.check_errors() == (0, 0) and fresh.check_errors() == (0, 0)
+        assert torch.equal(db.n_ids, fresh.n_ids)
+        assert torch.equal(db.ids, fresh.ids)
+        assert torch.equal(db.out, fresh.out)
+    db.scores.fill_(float("nan"))
+    db.score()
+    assert db.check_errors() == (0, 0)
+    ref = oracle_run(w)
+    gpu = {"scores": db.scores.cpu().numpy(), "ids": db.ids.cpu().numpy(), "n_ids": db.n_ids.cpu().numpy(),
+           "out": db.out.cpu().numpy()}
+    assert_scores_equal(w, gpu, ref)
+    assert_ids_equal(w, gpu, ref)
+    assert_attention_close(w, gpu, ref)

@@ -356,15 +356,15 @@ def test_decode_from_host_as_a_cuda_graph():
 def test_merge_path_does_not_change_bits():
     """An attention grid of more than one wave merges its runs in a second
     launch, a one-wave grid in its last CTA: the merge arithmetic is the same,
-    so a query's output in a 12-query batch (192 run CTAs) equals its
-    single-query decode (16 run CTAs) bit for bit."""
+    so a query's output in a 12-query batch (408 run CTAs, two per SM) equals
+    its single-query decode (34 run CTAs) bit for bit."""
     torch = need_gpu()
     from top_group_sparse_gb300 import qsa
     vis = [9001 + 1013 * i for i in range(11)] + [2052]
     w = wl.make_workload("merge", vis, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2, head_dim=128,
                          seed=97, slots="paged16")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert 8 * w.kv_heads * w.batch > sms  # the batch takes the two-launch merge
+    assert 17 * w.kv_heads * w.batch > 2 * sms  # the batch takes the two-launch merge
     db = qsa.DeviceBatch(w)
     db.decode()
     assert db.check_errors() == (0, 0)

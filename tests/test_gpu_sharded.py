@@ -27,8 +27,9 @@ def _shapes():
             dict(idx_heads=4, idx_dim=32, q_heads=4, kv_heads=4, head_dim=64)]
 
 
-def _states(db, rows, counts):
-    """qsa_attend_state over rows [B, <= row_cap] with counts [B]."""
+def _states(db, rows, counts, device=False):
+    """qsa_attend_state over rows [B, <= row_cap] with counts [B]: (acc, m, l)
+    as host arrays, or as the device tensors when device=True."""
     import torch
     from top_group_sparse_gb300 import qsa
     B = db.dims.batch
@@ -43,6 +44,8 @@ def _states(db, rows, counts):
     l = torch.full_like(m, float("nan"))
     qsa.qsa_attend_state(db.dims, db.inputs, ids, n_ids, acc, m, l, db.ws)
     assert db.check_errors() == (0, 0)
+    if device:
+        return acc, m, l
     return acc.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy()
 
 
@@ -54,8 +57,9 @@ def _vmax(w, b, ids):
 @pytest.mark.parametrize("shape", range(2))
 def test_state_of_the_whole_row_is_the_decode_output(shape):
     """acc / l of the whole emitted row is qsa_decode's output bit for bit
-    (the same runs, the same merge, the same division); an empty row gives
-    the empty state (m = -inf, l = 0, acc = 0)."""
+    (the same runs, the same merge, the same division), and so is that one
+    state passed through qsa_merge_states; an empty row gives the empty state
+    (m = -inf, l = 0, acc = 0) and a zero output."""
     torch = need_gpu()
     from top_group_sparse_gb300 import qsa
     w = wl.make_workload("state", [9001, 37, 2052, 0, 40003], seed=81, slots="paged16", **_shapes()[shape])
@@ -63,7 +67,12 @@ def test_state_of_the_whole_row_is_the_decode_output(shape):
     db.decode()
     torch.cuda.synchronize()
     ids, n, out = db.ids.cpu().numpy(), db.n_ids.cpu().numpy(), db.out.cpu().numpy()
-    acc, m, l = _states(db, ids, n)
+    acc_d, m_d, l_d = _states(db, ids, n, device=True)
+    acc, m, l = acc_d.cpu().numpy(), m_d.cpu().numpy(), l_d.cpu().numpy()
+    from top_group_sparse_gb300 import sharding as sh
+    one = sh.merge_states(db.dims, [(m_d, l_d, acc_d)])
+    torch.cuda.synchronize()
+    assert one.cpu().numpy().tobytes() == out.tobytes()
     for b in range(w.batch):
         if n[b] == 0:
             assert np.all(m[b] == -np.inf) and np.all(l[b] == 0) and not acc[b].any()
@@ -76,8 +85,8 @@ def test_state_of_the_whole_row_is_the_decode_output(shape):
 def test_row_slices_merge_to_the_row_attention():
     """Consecutive slices of each query's row (empty ones included), each
     attended on its own: every slice's state matches the oracle's state of
-    that slice, and the states merged in row order give the row's attention
-    within 1e-5 * max|V| of the oracle."""
+    that slice, and the states merged in row order by qsa_merge_states give
+    the row's attention within 1e-5 * max|V| of the oracle."""
     need_gpu()
     import oracle
     from top_group_sparse_gb300 import qsa
@@ -91,7 +100,9 @@ def test_row_slices_merge_to_the_row_attention():
     states = []
     for s in range(n_sl):
         sl = [rows[b][cuts[b][s]:cuts[b][s + 1]] for b in range(w.batch)]
-        states.append((sl, _states(db, sl, [len(x) for x in sl])))
+        states.append((sl, _states(db, sl, [len(x) for x in sl], device=True)))
+    merged_all = sh.merge_states(db.dims, [(m, l, acc) for _, (acc, m, l) in states]).cpu().numpy()
+    states = [(sl, tuple(t.cpu().numpy() for t in st)) for sl, st in states]
     for b in range(w.batch):
         vmax = _vmax(w, b, rows[b])
         slots_all = w.slot_map[w.slot_offset[b] + rows[b].astype(np.int64)]
@@ -106,8 +117,7 @@ def test_row_slices_merge_to_the_row_attention():
             assert np.abs(l[b] / pl - 1.0).max() <= 1e-5, (b, s)
             err = np.abs(acc[b] / l[b][:, None] - pacc / pl[:, None]).max() / vmax
             assert err <= ATTN_TOL, (b, s, err)
-        merged = sh.merge_partials([(m[b], l[b], acc[b]) for _, (acc, m, l) in states])
-        err = float(np.abs(merged.astype(np.float64) - ref["out"][b]).max()) / vmax
+        err = float(np.abs(merged_all[b].astype(np.float64) - ref["out"][b]).max()) / vmax
         assert err <= ATTN_TOL, (b, err)
 
 
@@ -156,8 +166,8 @@ def test_one_history_across_ranks_on_the_gpu(world):
     states = []
     for rg, last in ranges:
         sl = row[sh.rank_rows(row, rg.start, rg.stop, last)]
-        acc, m, l = _states(db, [sl], [len(sl)])
-        states.append((m[0], l[0], acc[0]))
-    out = sh.merge_partials(states)
+        acc, m, l = _states(db, [sl], [len(sl)], device=True)
+        states.append((m, l, acc))
+    out = sh.merge_states(db.dims, states).cpu().numpy()[0]
     err = float(np.abs(out.astype(np.float64) - ref["out"][0]).max()) / _vmax(w, 0, row)
     assert err <= ATTN_TOL, err

@@ -136,14 +136,14 @@ def test_partial_states_merge_to_the_sequential_softmax():
     slots = rng.permutation(S)[:513].astype(np.int32)
     scale = 1.0 / np.sqrt(d)
     ref = oracle.attend(q, kc, vc, slots, scale)
-    one = sh.merge_partials([oracle.attend_partial(q, kc, vc, slots, scale)])
+    one = oracle.merge_states([oracle.attend_partial(q, kc, vc, slots, scale)])
     assert one.tobytes() == ref.tobytes()
     tol = 1e-5 * float(np.abs(vc).max())
     for cuts in ([0, 513], [0, 200, 513], [0, 0, 100, 100, 400, 513], [0, 513, 513]):
         parts = [oracle.attend_partial(q, kc, vc, slots[a:b], scale) for a, b in zip(cuts, cuts[1:])]
-        got = sh.merge_partials(parts)
+        got = oracle.merge_states(parts)
         assert float(np.abs(got - ref).max()) <= tol, cuts
-    empty = sh.merge_partials([oracle.attend_partial(q, kc, vc, slots[:0], scale)])
+    empty = oracle.merge_states([oracle.attend_partial(q, kc, vc, slots[:0], scale)])
     assert not empty.any()
 
 
@@ -175,7 +175,7 @@ def _one_history_worker(rank, world, port, out_dir):
         part = oracle.attend_partial(w.q[0], w.k_cache, w.v_cache, slots, w.scale)
         parts = [None] * world
         dist.all_gather_object(parts, (rank, part))
-        out = sh.merge_partials([p for _, p in sorted(parts, key=lambda x: x[0])])
+        out = oracle.merge_states([p for _, p in sorted(parts, key=lambda x: x[0])])
         if rank == 0:
             ref = oracle.decode(w)
             n = int(ref["n_ids"][0])

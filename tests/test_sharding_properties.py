@@ -68,7 +68,7 @@ def test_states_of_row_cuts_merge_to_the_one_pass_softmax(n, cuts, gq, seed):
     ref = oracle.attend(q, kc, vc, slots, scale)
     bounds = [0] + sorted(min(c, n) for c in cuts) + [n]
     parts = [oracle.attend_partial(q, kc, vc, slots[a:b], scale) for a, b in zip(bounds, bounds[1:])]
-    got = sh.merge_partials(parts)
+    got = oracle.merge_states(parts)
     if n == 0:
         assert not got.any()
         return

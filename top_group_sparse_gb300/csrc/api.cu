@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "qsa_internal.cuh"
+#include "qsa_selftest.h"
 
 namespace qsa {
 
@@ -231,7 +232,10 @@ int32_t qsa_row_capacity(const qsa_dims *dims)
     return make_layout(dims).row_cap;
 }
 
-qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_stats *out)
+namespace {
+// pooled_rows < 0: the full-raw form; else the incremental form with a cache
+// of pooled_rows rows.
+qsa_status fill_stats(const qsa_dims *dims, const int32_t *visible_host, int64_t pooled_rows, qsa_stats *out)
 {
     if (!dims_valid(dims) || !out || (dims->batch > 0 && !visible_host)) return QSA_ERR_INVALID_ARG;
     qsa_stats st;
@@ -245,15 +249,28 @@ qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_
         st.candidate_groups += G;
         st.selected_groups += k;
         st.selected_tokens += W;
-        st.raw_key_bytes += T * dims->idx_dim * 4;
+        if (pooled_rows < 0) st.raw_key_bytes += T * dims->idx_dim * 4;
         st.kv_bytes += W * int64_t(dims->kv_heads) * dims->head_dim * 4 * 2;
     }
-    st.pooled_key_bytes = 0;
+    st.pooled_key_bytes = pooled_rows < 0 ? 0 : pooled_rows * dims->idx_dim * 4;
     st.workspace_bytes = int64_t(make_layout(dims).total);
     st.total_bytes = st.raw_key_bytes + st.kv_bytes + st.pooled_key_bytes + st.workspace_bytes;
-    st.dense_mask_bytes = 0;  // no query-by-key mask exists anywhere in this library
+    st.dense_mask_bytes = 0;  // no entry point allocates or writes a query-by-key mask
     *out = st;
     return QSA_OK;
+}
+}  // namespace
+
+qsa_status qsa_get_stats(const qsa_dims *dims, const int32_t *visible_host, qsa_stats *out)
+{
+    return fill_stats(dims, visible_host, -1, out);
+}
+
+qsa_status qsa_get_stats_pooled(const qsa_dims *dims, const int32_t *visible_host, int64_t pooled_rows,
+                                qsa_stats *out)
+{
+    if (pooled_rows < 0) return QSA_ERR_INVALID_ARG;
+    return fill_stats(dims, visible_host, pooled_rows, out);
 }
 
 const char *qsa_status_string(qsa_status status)
@@ -361,6 +378,26 @@ qsa_status qsa_gather_attend(const qsa_dims *dims, const qsa_inputs *in, const i
     return do_gather_attend(dims, in, ids, n_ids, k_scr, v_scr, out, ws, L, static_cast<cudaStream_t>(stream));
 }
 
+qsa_status qsa_selftest_copy_timeout(const qsa_dims *dims, const qsa_inputs *in, float *scores, void *ws,
+                                     size_t ws_bytes, uint64_t wait_ns, void *stream)
+{
+    if (!dims_valid(dims) || wait_ns == 0 || wait_ns > kWaitLimitNs) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, true, false)) != QSA_OK) return st;
+    if ((st = check_inputs_score(in)) != QSA_OK) return st;
+    if (!scores || !aligned(scores, 16)) return QSA_ERR_INVALID_ARG;
+    if ((st = check_ws(dims, ws, ws_bytes)) != QSA_OK) return st;
+    if (dims->batch == 0) return QSA_OK;
+    const Layout L = make_layout(dims);
+    const int sms = num_sms_of_current_device();
+    if (sms <= 0) return QSA_ERR_CUDA;
+    // equal shares (no per-SM weights), no copy issued, short waits
+    ScoreArgs a{in->q_idx, in->idx_keys, in->key_offset, in->visible, scores, L.score_stride,
+                dims->batch, dims->idx_heads, dims->idx_dim, dims->max_visible, err_word(ws, L),
+                ws_at<uint32_t>(ws, L.off_qmax), L.qmax_stride, nullptr, nullptr, nullptr, 0, 1, wait_ns};
+    return from_cuda(launch_score(a, sms, static_cast<cudaStream_t>(stream)));
+}
+
 qsa_status qsa_attend_state(const qsa_dims *dims, const qsa_inputs *in, const int32_t *ids, const int32_t *n_ids,
                             float *acc, float *m, float *l, void *ws, size_t ws_bytes, void *stream)
 {
@@ -376,6 +413,20 @@ qsa_status qsa_attend_state(const qsa_dims *dims, const qsa_inputs *in, const in
     const Layout L = make_layout(dims);
     return do_gather_attend(dims, in, ids, n_ids, nullptr, nullptr, acc, ws, L, static_cast<cudaStream_t>(stream),
                             false, nullptr, nullptr, m, l);
+}
+
+qsa_status qsa_merge_states(const qsa_dims *dims, int32_t n_parts, const float *m, const float *l, const float *acc,
+                            float *out, void *stream)
+{
+    if (!dims_valid(dims)) return QSA_ERR_INVALID_ARG;
+    qsa_status st;
+    if ((st = check_shapes(dims, false, true)) != QSA_OK) return st;
+    if (n_parts < 1 || !m || !l || !acc || !out) return QSA_ERR_INVALID_ARG;
+    if (!aligned(m, 4) || !aligned(l, 4) || !aligned(acc, 16) || !aligned(out, 16)) return QSA_ERR_INVALID_ARG;
+    const long long bh = (long long)dims->batch * dims->q_heads;
+    if (bh > 0x7fffffffLL / (long long)n_parts) return QSA_ERR_INVALID_ARG;
+    return from_cuda(launch_merge_states(m, l, acc, out, n_parts, int(bh), dims->head_dim,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -10,37 +10,39 @@
 // physical cache layout.
 //
 // GPU order (fixed, documented, batch independent).  The emitted row of
-// query b is cut into runs of kRowsPerPart consecutive rows, one CTA per
-// (run, query b, KV head); the cut depends only on n_ids[b].  A run is cut
-// into steps of 8 consecutive rows, and step j goes to warp j mod 12, which
+// query b is cut into runs of kRowsPerPart (128) consecutive rows, one CTA per
+// (run, KV head, query b); the cut depends only on n_ids[b].  A run is cut
+// into steps of 4 consecutive rows, and step j goes to warp j mod 8, which
 // keeps its own online-softmax state for the GQ query heads of the KV head:
 // per step, scaled scores x_i, the new running max m' = max(m, max x_i), the
 // rescale e^(m - m') of the denominator l and of the accumulator, then
 // l += sum_i e^(x_i - m') and acc += sum_i e^(x_i - m') v_i.  At the end of
-// the run the twelve warp states are merged in warp order (M = max m_w,
+// the run the eight warp states are merged in warp order (M = max m_w,
 // L = sum l_w e^(m_w - M), acc = sum acc_w e^(m_w - M)), and the runs are
 // merged in order the same way and divided by L (merge_runs): by the last CTA
 // of the (query, KV head) to finish -- an atomic ticket, nothing waits -- when
-// the grid is one wave, else by a second small launch after the grid, so that
-// no CTA holds its SM through the fence and the ticket.  With the state
-// export (AttendArgs::m_out) the merge stores M, L and the undivided acc
-// instead, so that separately attended slices of one row combine in row
+// the grid fits on the GPU at once, else by a second small launch after the
+// grid, so that no CTA holds its SM through the fence and the ticket.  With
+// the state export (AttendArgs::m_out) the merge stores M, L and the undivided
+// acc instead, so that separately attended slices of one row combine in row
 // order.  No floating-point atomics; the bits of a query's output do not
 // depend on the rest of the batch.
 //
 // Data movement: the CTA's threads resolve every row of its run at once
 // (one row each: the ID load, then the slot-map load).  Each warp then
-// streams only its own steps through its own two-slot ring in shared
-// memory with 16-byte asynchronous copies, one step ahead of its math, so no
-// thread-block barrier and no cross-warp wait sits inside the loop.
+// streams only its own steps through its own three-slot ring in shared
+// memory with 16-byte asynchronous copies, two steps ahead of its math, so no
+// thread-block barrier and no cross-warp wait sits inside the loop.  Eight
+// warps of short steps and two CTAs per SM (for GQ <= 8) keep sixteen warps
+// on every SM: the loop is issue- and latency-bound, and each warp has only
+// about four steps to run.
 //
-// Math of a step (8 rows x GQ heads).  Scores: lanes form HP = min(GQ, 4)
+// Math of a step (4 rows x GQ heads).  Scores: lanes form HP = min(GQ, 4)
 // head groups of DS = 32/HP lanes; a lane holds HPL = GQ/HP heads of the query
 // in registers, restricted to its d-slice (16-byte columns ds, ds + DS, ...),
-// forms 8 x HPL partial dot products, and a reduce-scatter over the DS lanes
-// of its group leaves it the finished dots of one row (ds, for GQ >= 4) and
-// its HPL heads.  Weighted values: a lane owns one 16-byte column of V for
-// all GQ heads.
+// forms 4 x HPL partial dot products, and a reduce-scatter over the DS lanes
+// of its group leaves it NVO finished dots (one row, NVO consecutive heads).
+// Weighted values: a lane owns one 16-byte column of V for all GQ heads.
 //
 // Row source: Src::kScratch reads the gathered scratch (qsa_attend);
 // Src::kCache resolves each ID through the slot map and copies the row from
@@ -55,12 +57,18 @@
 namespace qsa {
 namespace {
 
-constexpr int kRowsPerPart = kAttendRowsPerPart;
-constexpr int kParts = kAttendParts;               // 8 runs at most (2,051 rows)
-constexpr int kStepRows = 8;                       // rows per warp step
-constexpr int kRing = 2;                           // steps in flight per warp (ring slots)
-constexpr int kWarps = 12;
+constexpr int kRowsPerPart = kAttendRowsPerPart;  // 128
+constexpr int kParts = kAttendParts;               // 17 runs at most (2,051 rows)
+constexpr int kStepRows = 4;                       // rows per warp step
+constexpr int kRing = 3;                           // steps in flight per warp (ring slots)
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+
+// CTAs per SM the kernel is built for: the running state of GQ heads (an
+// accumulator column and the query slice per head) fits 128 registers a
+// thread up to GQ = 8.
+template <int GQ>
+constexpr int attend_ctas_per_sm() { return GQ <= 8 ? 2 : 1; }
 
 enum class Src { kScratch, kCache, kCacheStore };
 
@@ -68,7 +76,7 @@ template <int D, int GQ>
 struct AttendSmem {
     // every array read or written as float4 (or by 16-byte async copies)
     // starts on a 16-byte boundary whatever GQ and D are
-    alignas(128) float k[kWarps][kRing][kStepRows][D];  // also the end-of-run reduction area
+    alignas(128) float k[kWarps][kRing][kStepRows][D];  // k and v: also the end-of-run reduction area
     alignas(128) float v[kWarps][kRing][kStepRows][D];
     alignas(16) float q[GQ][D];
     alignas(16) float pt[kWarps][kStepRows][GQ < 4 ? 4 : GQ];  // weights of a warp's step, [row][head]
@@ -192,6 +200,36 @@ __device__ __forceinline__ void merge_runs(const AttendArgs &a, int b, int kvh, 
 
 constexpr int kMergeThreads = 256;
 
+// qsa_merge_states: the states of n_parts consecutive slices of each row
+// (m, l [n_parts, bh]; acc [n_parts, bh, D]) merged in slice order with the
+// arithmetic of merge_runs -- M = max m_r, w_r = e^(m_r - M), L and acc
+// summed by fmaf in slice order, then acc / L -- so that one slice of a whole
+// row gives qsa_decode's output bit for bit.  One thread per (query-head,
+// 16-byte column).
+__global__ void __launch_bounds__(kMergeThreads)
+merge_states_kernel(const float *m, const float *l, const float *acc, float *out, int n_parts, int bh, int f4)
+{
+    const int64_t e = int64_t(blockIdx.x) * kMergeThreads + threadIdx.x;
+    if (e >= int64_t(bh) * f4) return;
+    const int hb = int(e / f4), j4 = int(e - int64_t(hb) * f4);
+    float M = -INFINITY;
+    for (int r = 0; r < n_parts; ++r) M = fmaxf(M, __ldg(m + int64_t(r) * bh + hb));
+    float L = 0.0f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < n_parts; ++r) {
+        const float w = M == -INFINITY ? 0.0f : expf(__ldg(m + int64_t(r) * bh + hb) - M);
+        L = fmaf(__ldg(l + int64_t(r) * bh + hb), w, L);
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(acc) + (int64_t(r) * bh + hb) * f4 + j4);
+        o.x = fmaf(x.x, w, o.x);
+        o.y = fmaf(x.y, w, o.y);
+        o.z = fmaf(x.z, w, o.z);
+        o.w = fmaf(x.w, w, o.w);
+    }
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (L > 0.0f) res = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+    reinterpret_cast<float4 *>(out)[e] = res;
+}
+
 // The second launch of a deferred merge: one CTA per (KV head, query).
 template <int D, int GQ>
 __global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const AttendArgs a)
@@ -207,7 +245,7 @@ __global__ void __launch_bounds__(kMergeThreads) attend_merge_kernel(const Atten
 }
 
 template <int D, int GQ, Src kSrc>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, attend_ctas_per_sm<GQ>())
 attend_kernel(const AttendArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -223,8 +261,13 @@ attend_kernel(const AttendArgs a)
     constexpr int DS = 32 / HP;
     constexpr int NF = (F4 + DS - 1) / DS;
     constexpr int NV = kStepRows * HPL;          // partial dots per lane before the reduce
-    constexpr int RSH = DS / kStepRows;          // lanes sharing a row after the reduce (>= 1)
-    static_assert(NV <= 32 && (NV >= DS ? NV / DS == HPL : HPL == 1), "one row per lane after the reduce");
+    // after the reduce-scatter a lane holds NVO finished dots, entries
+    // (ds / RSH) * NVO + j of the [row][head] list (RSH lanes hold each copy):
+    // one row, heads u0 .. u0 + NVO - 1; lanes ROFF apart hold the next row
+    constexpr int NVO = NV >= DS ? NV / DS : 1;
+    constexpr int RSH = NV >= DS ? 1 : DS / NV;
+    constexpr int ROFF = (HPL / NVO) * RSH;
+    static_assert(NV <= 32 && HPL % NVO == 0 && ROFF * kStepRows == DS, "one row per lane after the reduce");
 
     const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -299,7 +342,7 @@ attend_kernel(const AttendArgs a)
     }
     __syncthreads();
 
-    // ---- this warp's steps: j = warp, warp + 8, ... ---------------------------------
+    // ---- this warp's steps: j = warp, warp + kWarps, ... ----------------------------
     const int nsteps = (r_end - r0 + kStepRows - 1) / kStepRows;
     const int my_steps = nsteps > warp ? (nsteps - warp + kWarps - 1) / kWarps : 0;
     const float *ksrc = kFromCache ? a.k_cache : a.k_scr;
@@ -329,7 +372,9 @@ attend_kernel(const AttendArgs a)
 
     // score-layout coordinates of this lane
     const int hg = lane / DS, ds = lane % DS;
-    const int r_lane = ds / RSH;                 // the row whose dots this lane ends with
+    const int i0 = (ds / RSH) * NVO;             // first [row][head] entry this lane ends with
+    const int r_lane = i0 / HPL;                 // its row
+    const int h_lane = hg * HPL + i0 % HPL;      // its first head (NVO consecutive heads)
     float4 qreg[HPL][NF];
 #pragma unroll
     for (int u = 0; u < HPL; ++u)
@@ -343,11 +388,11 @@ attend_kernel(const AttendArgs a)
     float4 acc[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float m_run[HPL], l_run[HPL];  // states of heads hg*HPL + u over this warp's rows
+    float m_run[NVO], l_run[NVO];  // states of heads h_lane + j over this warp's rows
 #pragma unroll
-    for (int u = 0; u < HPL; ++u) {
-        m_run[u] = -INFINITY;
-        l_run[u] = 0.0f;
+    for (int j = 0; j < NVO; ++j) {
+        m_run[j] = -INFINITY;
+        l_run[j] = 0.0f;
     }
 
     for (int k = 0; k < my_steps; ++k) {
@@ -369,7 +414,7 @@ attend_kernel(const AttendArgs a)
             }
         }
 
-        // ---- 8 rows x HPL heads of partial dots over this lane's columns --------------
+        // ---- 4 rows x HPL heads of partial dots over this lane's columns --------------
         float v[32];
 #pragma unroll
         for (int r = 0; r < kStepRows; ++r) {
@@ -388,36 +433,36 @@ attend_kernel(const AttendArgs a)
                 }
             }
         }
-        reduce_scatter<NV, DS / 2>(v, lane);  // v[u]: row r_lane, head hg*HPL + u
+        reduce_scatter<NV, DS / 2>(v, lane);  // v[j]: row r_lane, head h_lane + j
 
-        // ---- online softmax step of this lane's heads over the 8 rows ------------------
-        float al[HPL];
+        // ---- online softmax step of this lane's heads over the 4 rows ------------------
+        float al[NVO];
         bool unit = true;  // every rescale factor is 1 (nothing to rescale)
 #pragma unroll
-        for (int u = 0; u < HPL; ++u) {
-            const bool ok = r_lane < rows && hg * HPL + u < gq;
-            const float x = ok ? a.scale * v[u] : -INFINITY;
+        for (int j = 0; j < NVO; ++j) {
+            const bool ok = r_lane < rows && h_lane + j < gq;
+            const float x = ok ? a.scale * v[j] : -INFINITY;
             float mc = x;
 #pragma unroll
-            for (int o = RSH; o < DS; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-            const float m_new = fmaxf(m_run[u], mc);
+            for (int o = ROFF; o < DS; o <<= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+            const float m_new = fmaxf(m_run[j], mc);
             float p = 0.0f, alpha = 0.0f;
             if (m_new != -INFINITY) {
                 p = expf(x - m_new);
-                alpha = m_run[u] == -INFINITY ? 0.0f : expf(m_run[u] - m_new);
+                alpha = m_run[j] == -INFINITY ? 0.0f : expf(m_run[j] - m_new);
             }
             float ps = p;
 #pragma unroll
-            for (int o = RSH; o < DS; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            l_run[u] = fmaf(l_run[u], alpha, ps);
-            m_run[u] = m_new;
-            al[u] = alpha;
+            for (int o = ROFF; o < DS; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            l_run[j] = fmaf(l_run[j], alpha, ps);
+            m_run[j] = m_new;
+            al[j] = alpha;
             unit = unit && (alpha == 1.0f || m_new == -INFINITY);
-            if (ds % RSH == 0) sm.pt[warp][r_lane][hg * HPL + u] = p;
+            if (ds % RSH == 0) sm.pt[warp][r_lane][h_lane + j] = p;
         }
-        if (ds == 0) {
+        if (r_lane == 0 && ds % RSH == 0) {
 #pragma unroll
-            for (int u = 0; u < HPL; ++u) sm.alpha[warp][hg * HPL + u] = al[u];
+            for (int j = 0; j < NVO; ++j) sm.alpha[warp][h_lane + j] = al[j];
         }
         const bool rescale = !__all_sync(0xffffffffu, unit);
         __syncwarp();
@@ -470,17 +515,17 @@ attend_kernel(const AttendArgs a)
 
     // ---- this CTA's partial: the warp states merged in warp order --------------------
     __syncthreads();  // every warp is done with its ring: it becomes the reduction area
-    float *red = &sm.k[0][0][0][0];  // [kWarps][GQ][D]
+    float *red = &sm.k[0][0][0][0];  // [kWarps][GQ][D], over k and then v
     if (col) {
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh)
             *reinterpret_cast<float4 *>(&red[(warp * GQ + hh) * D + 4 * lane]) = acc[hh];
     }
-    if (ds == 0) {
+    if (r_lane == 0 && ds % RSH == 0) {
 #pragma unroll
-        for (int u = 0; u < HPL; ++u) {
-            sm.wm[warp][hg * HPL + u] = m_run[u];
-            sm.wl[warp][hg * HPL + u] = l_run[u];
+        for (int j = 0; j < NVO; ++j) {
+            sm.wm[warp][h_lane + j] = m_run[j];
+            sm.wl[warp][h_lane + j] = l_run[j];
         }
     }
     __syncthreads();
@@ -544,19 +589,21 @@ cudaError_t launch_attend_t(const AttendArgs &a, cudaStream_t s, bool pdl)
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    static int sms[64] = {};
-    if (sms[dev] == 0) {
-        int n = 0;
+    static long long resident[64] = {};  // CTAs of this kernel the GPU holds at once
+    if (resident[dev] == 0) {
+        int n = 0, per_sm = 0;
         cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        sms[dev] = n > 0 ? n : 1;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<D, GQ, kSrc>, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        resident[dev] = (long long)(n > 0 ? n : 1) * (per_sm > 0 ? per_sm : 1);
     }
     const dim3 grid(kParts, unsigned(a.kv_heads), unsigned(a.batch));
-    // One CTA fits an SM: in a grid of more than one wave every CTA would
-    // hold its SM through the merge's fence and ticket, so the runs' states
-    // are merged by a second launch instead (same arithmetic, same bits).
+    // In a grid of more than one wave every CTA would hold its SM through the
+    // merge's fence and ticket, so the runs' states are merged by a second
+    // launch instead (same arithmetic, same bits).
     AttendArgs ad = a;
-    ad.defer_merge = (long long)kParts * a.kv_heads * a.batch > sms[dev] ? 1 : 0;
+    ad.defer_merge = (long long)kParts * a.kv_heads * a.batch > resident[dev] ? 1 : 0;
     cudaError_t e = launch_kernel(attend_kernel<D, GQ, kSrc>, grid, dim3(kThreads), smem, s, pdl, ad);
     if (e != cudaSuccess || !ad.defer_merge) return e;
     return launch_kernel(attend_merge_kernel<D, GQ>, dim3(unsigned(a.kv_heads), unsigned(a.batch)),
@@ -583,6 +630,7 @@ cudaError_t launch_attend_src(const AttendArgs &a, cudaStream_t s, bool pdl)
 }
 
 static_assert(sizeof(AttendSmem<128, 16>) <= 227 * 1024, "shared memory per CTA");
+static_assert(2 * (sizeof(AttendSmem<128, 8>) + 1024) <= 228 * 1024, "two CTAs per SM up to GQ = 8");
 static_assert(kRowsPerPart <= kThreads, "one thread per row of the run resolves it");
 static_assert(kParts * kRowsPerPart >= kGroup * QSA_MAX_BUDGET + kGroup - 1, "runs cover the longest row");
 static_assert(kRowsPerPart % kStepRows == 0, "runs are whole steps");
@@ -593,7 +641,8 @@ constexpr bool layout_ok()
     using S = AttendSmem<D, GQ>;
     return offsetof(S, k) % 16 == 0 && offsetof(S, v) % 16 == 0 && offsetof(S, q) % 16 == 0 &&
            offsetof(S, pt) % 16 == 0 && offsetof(S, alpha) % 16 == 0 && offsetof(S, off) % 8 == 0 &&
-           (D * 4) % 16 == 0 && sizeof(S::k) >= size_t(kWarps) * GQ * D * 4;  // room for the reduction
+           (D * 4) % 16 == 0 && offsetof(S, v) == offsetof(S, k) + sizeof(S::k) &&
+           sizeof(S::k) + sizeof(S::v) >= size_t(kWarps) * GQ * D * 4;  // room for the reduction
 }
 static_assert(layout_ok<64, 1>() && layout_ok<64, 2>() && layout_ok<64, 4>() && layout_ok<64, 8>() &&
                   layout_ok<64, 16>() && layout_ok<128, 1>() && layout_ok<128, 2>() && layout_ok<128, 4>() &&
@@ -607,6 +656,17 @@ bool attend_shape_supported(int head_dim, int q_heads, int kv_heads)
     if (head_dim != 64 && head_dim != 128) return false;
     if (kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0) return false;
     return q_heads / kv_heads <= kMaxGqa;
+}
+
+cudaError_t launch_merge_states(const float *m, const float *l, const float *acc, float *out, int n_parts,
+                                int bh, int head_dim, cudaStream_t s)
+{
+    const int f4 = head_dim / 4;
+    const long long n = (long long)bh * f4;
+    if (n == 0) return cudaSuccess;
+    const unsigned grid = unsigned((n + kMergeThreads - 1) / kMergeThreads);
+    merge_states_kernel<<<grid, kMergeThreads, 0, s>>>(m, l, acc, out, n_parts, bh, f4);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl)

@@ -13,9 +13,12 @@
 // names a host-side stand-in), so the first call on each device, with that
 // device current, asks the runtime for the array's device address with
 // cudaGetSymbolAddress and keeps it.  That first call should therefore come
-// before any stream capture.  All calls share the array: the counters that
-// must start at zero are cleared on the stream at every call, and calls that
-// overlap on the GPU race with each other.
+// before any stream capture.  The kept address is valid for as long as the
+// device's context lives: after a cudaDeviceReset the device code may load at
+// another address, so the call is not for use after a reset.  All calls
+// share the array: the counters that must start at zero are cleared on the
+// stream at every call, and calls that overlap on the GPU race with each
+// other.
 #include <cuda_runtime.h>
 
 #include <mutex>

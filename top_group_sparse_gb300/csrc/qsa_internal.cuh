@@ -17,9 +17,9 @@ namespace qsa {
 // ---- workspace layout -----------------------------------------------------
 
 constexpr int kGroup = 4;            // tokens per scored group
-constexpr int kAttendRowsPerPart = 264;  // emitted rows per attention CTA (33 steps of 8)
+constexpr int kAttendRowsPerPart = 128;  // emitted rows per attention CTA (32 steps of 4)
 constexpr int kAttendParts =             // attention CTAs (and partials) per (query, KV head) at
-    (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 8
+    (kGroup * QSA_MAX_BUDGET + kGroup - 1 + kAttendRowsPerPart - 1) / kAttendRowsPerPart;  // most: 17
 constexpr int kMaxGqa = 16;          // q heads per KV head supported by attend
 
 // The raw scorer's per-SM balance (in the workspace; all zero at first).
@@ -99,6 +99,10 @@ struct ScoreArgs {
     // raw keys only: the per-SM balance (nullptr: equal shares per CTA)
     ScoreBalance *bal;
     int32_t bal_coop;        // set by the launcher: a cooperative launch, two CTAs on every SM
+    // the failure-detection self-test: the producer issues no copy (no_issue)
+    // and each copy wait gives up after wait_ns (0: the normal limit)
+    int32_t no_issue;
+    uint64_t wait_ns;
 };
 bool score_shape_supported(int idx_heads, int idx_dim);
 cudaError_t launch_score(const ScoreArgs &a, int num_sms, cudaStream_t s);
@@ -190,6 +194,9 @@ struct AttendArgs {
 };
 bool attend_shape_supported(int head_dim, int q_heads, int kv_heads);
 cudaError_t launch_attend(const AttendArgs &a, cudaStream_t s, bool pdl = false);
+// states [n_parts, bh] (m, l) and [n_parts, bh, head_dim] (acc) -> out [bh, head_dim]
+cudaError_t launch_merge_states(const float *m, const float *l, const float *acc, float *out, int n_parts,
+                                int bh, int head_dim, cudaStream_t s);
 
 // ---- device helpers ---------------------------------------------------------
 

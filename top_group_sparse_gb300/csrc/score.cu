@@ -210,7 +210,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         ++t_issue;
         ++n_issued;
     };
-    if (tid == 0)
+    if (tid == 0 && !a.no_issue)
         for (int s = 0; s < C::kStages; ++s) issue(s);
 
     float qreg[D];
@@ -241,7 +241,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
             cur_b = r.b;
         }
 
-        const bool ok = mbar_wait_bounded(&full[s], parity, kWaitLimitNs);
+        const bool ok = mbar_wait_bounded(&full[s], parity, a.wait_ns != 0 ? a.wait_ns : kWaitLimitNs);
 
         if constexpr (!kPooled) {
             // Pool, 16 bytes per item: item e is (group e / F4, chunk e % F4).
@@ -259,7 +259,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
                 timed_out = true;
                 break;
             }
-            if (tid == 0) issue(s);  // refill stage s with the tile kStages ahead
+            if (tid == 0 && !a.no_issue) issue(s);  // refill stage s with the tile kStages ahead
         }
         // (the pooled form reads its stage in place: one barrier per tile,
         // after the dots, settles a timed-out wait and frees the stage)
@@ -296,7 +296,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
                 timed_out = true;
                 break;
             }
-            if (tid == 0) issue(s);
+            if (tid == 0 && !a.no_issue) issue(s);
         }
         const int base = lane & ~(H - 1);
 #pragma unroll
@@ -323,7 +323,9 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         ++it;
     }
 
-    if (bal && tid == 0 && s_bal[2] >= 0) {  // this CTA's time, for the next launch's weights
+    // this CTA's time, for the next launch's weights (a launch whose waits ran
+    // out measured nothing about the SM's speed)
+    if (bal && tid == 0 && s_bal[2] >= 0 && !timed_out) {
         const uint64_t dt = global_timer_ns() - t_start;
         a.bal->el_ns[s_bal[2] >> 1][s_bal[2] & 1] = uint32_t(dt < 0xffffffffull ? dt : 0xffffffffull);
         a.bal->tiles[s_bal[2] >> 1][s_bal[2] & 1] = uint32_t(t_end - t_begin);

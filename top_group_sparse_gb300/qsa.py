@@ -15,9 +15,9 @@ import numpy as np
 
 __all__ = [
     "QsaError", "QsaDims", "QsaInputs", "QsaStats", "load", "library_path", "exported_symbols",
-    "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats",
+    "qsa_workspace_size", "qsa_score_stride", "qsa_row_capacity", "qsa_get_stats", "qsa_get_stats_pooled",
     "qsa_status_string", "qsa_workspace_init", "qsa_check_errors", "qsa_score_groups",
-    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_attend_state", "qsa_decode",
+    "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend", "qsa_attend_state", "qsa_merge_states", "qsa_selftest_copy_timeout", "qsa_decode",
     "qsa_decode_profiled", "qsa_attend_noalloc", "qsa_pool_groups", "qsa_score_pooled",
     "qsa_decode_pooled", "qsa_score_groups_shared", "qsa_decode_shared", "qsa_probe_ffma",
     "make_dims",
@@ -96,6 +96,8 @@ def load(path: str | None = None):
     L.qsa_row_capacity.restype = ctypes.c_int32
     L.qsa_get_stats.argtypes = [_DP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(QsaStats)]
     L.qsa_get_stats.restype = ctypes.c_int
+    L.qsa_get_stats_pooled.argtypes = [_DP, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64, ctypes.POINTER(QsaStats)]
+    L.qsa_get_stats_pooled.restype = ctypes.c_int
     L.qsa_status_string.argtypes = [ctypes.c_int]
     L.qsa_status_string.restype = ctypes.c_char_p
     L.qsa_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
@@ -114,6 +116,10 @@ def load(path: str | None = None):
     L.qsa_gather_attend.restype = ctypes.c_int
     L.qsa_attend_state.argtypes = [_DP, _IP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_attend_state.restype = ctypes.c_int
+    L.qsa_merge_states.argtypes = [_DP, ctypes.c_int32, _P, _P, _P, _P, _P]
+    L.qsa_selftest_copy_timeout.argtypes = [_DP, _IP, _P, _P, ctypes.c_size_t, ctypes.c_uint64, _P]
+    L.qsa_selftest_copy_timeout.restype = ctypes.c_int
+    L.qsa_merge_states.restype = ctypes.c_int
     L.qsa_decode.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.qsa_decode.restype = ctypes.c_int
     L.qsa_decode_profiled.argtypes = [_DP, _IP, _P, _P, _P, _P, ctypes.c_size_t, _P,
@@ -139,7 +145,7 @@ def load(path: str | None = None):
 
 
 def exported_symbols(header: str | None = None) -> list[str]:
-    """Names of the functions include/qsa.h declares."""
+    """Names of the functions include/qsa.h (or the given header) declares."""
     import re
     header = header or os.path.join(os.path.dirname(_PKG), "include", "qsa.h")
     text = open(header).read()
@@ -209,6 +215,15 @@ def qsa_get_stats(dims: QsaDims, visible_host) -> dict:
     return st.as_dict()
 
 
+def qsa_get_stats_pooled(dims: QsaDims, visible_host, pooled_rows: int) -> dict:
+    vis = np.ascontiguousarray(np.asarray(visible_host, dtype=np.int32))
+    st = QsaStats()
+    _check("qsa_get_stats_pooled", load().qsa_get_stats_pooled(
+        ctypes.byref(dims), vis.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(pooled_rows),
+        ctypes.byref(st)))
+    return st.as_dict()
+
+
 def qsa_status_string(status: int) -> str:
     return load().qsa_status_string(int(status)).decode()
 
@@ -269,6 +284,21 @@ def qsa_attend_state(dims, inputs, ids, n_ids, acc, m, l, ws, stream=None) -> in
     return _check("qsa_attend_state", load().qsa_attend_state(
         ctypes.byref(dims), ctypes.byref(inputs), _ptr(ids), _ptr(n_ids), _ptr(acc), _ptr(m), _ptr(l),
         p, n, _stream(stream)))
+
+
+def qsa_selftest_copy_timeout(dims, inputs, scores, ws, wait_ns, stream=None) -> int:
+    """The failure-detection self-test (include/qsa_selftest.h): the raw scorer
+    with no copy issued, so that every CTA's bounded wait runs out after wait_ns."""
+    p, n = _ws(ws)
+    return _check("qsa_selftest_copy_timeout", load().qsa_selftest_copy_timeout(
+        ctypes.byref(dims), ctypes.byref(inputs), _ptr(scores), p, n, int(wait_ns), _stream(stream)))
+
+
+def qsa_merge_states(dims, n_parts, m, l, acc, out, stream=None) -> int:
+    """Output [B, n_q, d] of rows whose consecutive slices' states are
+    m, l [n_parts, B, n_q] and acc [n_parts, B, n_q, d], merged in slice order."""
+    return _check("qsa_merge_states", load().qsa_merge_states(
+        ctypes.byref(dims), int(n_parts), _ptr(m), _ptr(l), _ptr(acc), _ptr(out), _stream(stream)))
 
 
 def qsa_decode(dims, inputs, ids, n_ids, out, ws, stream=None) -> int:

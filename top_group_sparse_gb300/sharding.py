@@ -46,8 +46,9 @@ def max_over_ranks(value: float, device=None) -> float:
 #   3. the emitted row (chosen groups ascending, x4, then the tail) is the same
 #      on every rank; the rows of rank r form one contiguous slice of it, and
 #      rank order is time order;
-#   4. each rank runs the online softmax over its slice, in order, and the
-#      per-rank states (m, l, acc) are merged in ascending rank order.
+#   4. each rank runs the online softmax over its slice, in order
+#      (qsa_attend_state), and the per-rank states (m, l, acc) are merged in
+#      ascending rank order (qsa_merge_states).
 
 
 def shard_groups(n_groups: int, world: int, rank: int) -> range:
@@ -113,22 +114,18 @@ def rank_rows(ids, g_lo: int, g_hi: int, last: bool) -> slice:
     return slice(start, stop)
 
 
-def merge_partials(parts):
-    """Output [n_q, d] from per-rank online-softmax states (m [n_q], l [n_q],
-    acc [n_q, d]) given in ascending rank (time) order; binary32 throughout,
-    an empty state (m = -inf, l = 0) contributes nothing, an empty row gives 0."""
-    import numpy as np
-    m = np.array(parts[0][0], np.float32)
-    l = np.array(parts[0][1], np.float32)
-    acc = np.array(parts[0][2], np.float32)
-    with np.errstate(invalid="ignore", over="ignore"):
-        for m2, l2, a2 in parts[1:]:
-            m2 = np.asarray(m2, np.float32)
-            mn = np.maximum(m, m2)
-            s1 = np.where(m == -np.inf, np.float32(0.0), np.exp(m - mn)).astype(np.float32)
-            s2 = np.where(m2 == -np.inf, np.float32(0.0), np.exp(m2 - mn)).astype(np.float32)
-            l = (l * s1 + np.asarray(l2, np.float32) * s2).astype(np.float32)
-            acc = (acc * s1[:, None] + np.asarray(a2, np.float32) * s2[:, None]).astype(np.float32)
-            m = mn
-        out = np.where(l[:, None] > 0, acc / np.where(l > 0, l, np.float32(1.0))[:, None], np.float32(0.0))
-    return out.astype(np.float32)
+def merge_states(dims, states, stream=None):
+    """The attention output [B, n_q, d] of rows whose consecutive slices were
+    attended apart (one slice per rank), from the slices' online-softmax
+    states in row (rank) order: states = [(m [B, n_q], l [B, n_q],
+    acc [B, n_q, d]), ...], device tensors as qsa_attend_state returns them.
+    The merge itself runs in the library (qsa_merge_states); here the states
+    are only stacked into the layout it takes."""
+    import torch
+    from . import qsa
+    m = torch.stack([st[0] for st in states]).contiguous()
+    l = torch.stack([st[1] for st in states]).contiguous()
+    acc = torch.stack([st[2] for st in states]).contiguous()
+    out = torch.empty_like(states[0][2])
+    qsa.qsa_merge_states(dims, len(states), m, l, acc, out, stream)
+    return out
