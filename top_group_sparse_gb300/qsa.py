@@ -471,6 +471,23 @@ class DeviceBatch:
         h_out = torch.empty(self.step_out.shape, dtype=torch.uint8).pin_memory()
         return h_in, h_out
 
+    def step_slot(self):
+        """A second device buffer laid out like step_in (holding the same step
+        inputs) and the QsaInputs that point into it -- the history, the K/V
+        caches and the slot map stay shared -- so that two host-driven steps
+        can be in flight at once: one step's inputs copied in while the other
+        step's kernels run.  Returns (buffer, inputs)."""
+        buf = self.step_in.clone()
+        base = self.step_in.data_ptr()
+
+        def at(t):
+            return buf.data_ptr() + (t.data_ptr() - base)
+
+        inp = QsaInputs(at(self.q_idx), _ptr(self.idx_keys), at(self.key_offset), at(self.visible), at(self.q),
+                        _ptr(self.k_cache), _ptr(self.v_cache), int(self.inputs.num_slots), _ptr(self.slot_map),
+                        at(self.slot_offset))
+        return buf, inp
+
     def decode_from_host(self, h_in, h_out, stream=None):
         """One step on the current torch stream (or `stream`): the step's
         inputs from h_in, qsa_decode, the ID rows, counts and outputs to
