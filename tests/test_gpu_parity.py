@@ -353,24 +353,53 @@ def test_decode_from_host_as_a_cuda_graph():
     assert db.check_errors() == (0, 0)
 
 
-def test_merge_path_does_not_change_bits():
+@pytest.mark.parametrize("q_heads,kv_heads,head_dim,nq", [(16, 2, 128, 12), (16, 1, 64, 40), (4, 4, 128, 30)])
+def test_merge_path_does_not_change_bits(q_heads, kv_heads, head_dim, nq):
     """An attention grid of more than one wave merges its runs in a second
-    launch, a one-wave grid in its last CTA: the merge arithmetic is the same,
-    so a query's output in a 12-query batch (408 run CTAs, two per SM) equals
-    its single-query decode (34 run CTAs) bit for bit."""
+    launch, a one-wave grid in its last CTA: the merge arithmetic is the
+    same, so a query's output in a batch of several waves equals its
+    single-query decode bit for bit -- for one and two CTAs per SM (GQ 16,
+    8 and 1; head dims 64 and 128), with rows of every length (runs without
+    rows among them) and grids of up to seven waves."""
     torch = need_gpu()
     from top_group_sparse_gb300 import qsa
-    vis = [9001 + 1013 * i for i in range(11)] + [2052]
-    w = wl.make_workload("merge", vis, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2, head_dim=128,
-                         seed=97, slots="paged16")
+    vis = [9001 + 1013 * (i % 11) for i in range(nq - 3)] + [2052, 40, 700]
+    w = wl.make_workload("merge", vis, idx_heads=8, idx_dim=64, q_heads=q_heads, kv_heads=kv_heads,
+                         head_dim=head_dim, seed=97 + nq, slots="paged16")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert 17 * w.kv_heads * w.batch > 2 * sms  # the batch takes the two-launch merge
+    per_sm = 2 if q_heads // kv_heads <= 8 else 1
+    assert 17 * w.kv_heads * w.batch > per_sm * sms  # the batch takes the persistent grid
     db = qsa.DeviceBatch(w)
     db.decode()
     assert db.check_errors() == (0, 0)
     out = db.out.cpu().numpy()
-    for b in (0, 5, 11):
+    ids, n_ids = db.ids.cpu().numpy(), db.n_ids.cpu().numpy()
+    for b in sorted({0, 5, nq - 3, nq - 2, nq - 1}):
         one = qsa.DeviceBatch(w, queries=[b])
         one.decode()
         assert one.check_errors() == (0, 0)
+        assert one.out.cpu().numpy()[0].tobytes() == out[b].tobytes(), b
+        assert int(one.n_ids[0]) == n_ids[b]
+        assert np.array_equal(one.ids.cpu().numpy()[0, : n_ids[b]], ids[b, : n_ids[b]])
+
+
+def test_multi_wave_grid_flags_a_bad_row_and_keeps_the_rest():
+    """A query whose visible length exceeds the bound, inside a batch of
+    several attention waves: its row is empty, its output zero and the
+    error word flagged; every other query equals its single-query decode."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    vis = [6000 + 517 * i for i in range(12)]
+    w = wl.make_workload("pbad", vis, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2, head_dim=128,
+                         seed=131, slots="paged16")
+    db = qsa.DeviceBatch(w)
+    db.visible[4] = w.max_visible + 1
+    db.decode()
+    st, flags = db.check_errors()
+    assert st == qsa.QSA_ERR_DEVICE_FAULT and flags & qsa.QSA_DEVERR_VISIBLE_RANGE
+    assert int(db.n_ids[4]) == 0 and bool(torch.all(db.out[4] == 0))
+    out = db.out.cpu().numpy()
+    for b in (0, 3, 5, 11):
+        one = qsa.DeviceBatch(w, queries=[b])
+        one.decode()
         assert one.out.cpu().numpy()[0].tobytes() == out[b].tobytes(), b
