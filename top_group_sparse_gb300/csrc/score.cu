@@ -31,6 +31,8 @@
 // groups complete): then a stage holds pooled rows, already in the swizzled
 // tile layout (the cache is stored that way), the dots read the stage in
 // place, and the stream is G * D * 4 bytes per query instead of T * D * 4.
+// There a thread holds two heads of q and runs their chains for H/2 groups
+// of the tile, so each 16-byte shared load feeds 8 FMAs.
 // pool_groups_kernel fills that cache with the very
 // pooling arithmetic of the raw path (pool4 below), so both forms give the
 // same scores bit for bit -- the full-raw / incremental identity.
@@ -43,11 +45,14 @@ namespace {
 template <int H, int D, bool kPooled>
 struct ScoreCfg {
     // The pooled form moves 4x fewer bytes per group, so FMA latency, not
-    // HBM, sets its pace: small CTAs (three per SM) whose threads each run
-    // eight independent FMA chains per tile.
+    // HBM, sets its pace: small CTAs (three per SM) whose threads hold two
+    // heads of q (each 16-byte shared load feeds 8 FMAs) and run H
+    // independent FMA chains per tile (H/2 groups x 2 heads).
     static constexpr int kThreads = kPooled ? 128 : 256;
-    static constexpr int kGPT = kPooled ? 8 : 1;            // groups per thread per tile
-    static constexpr int kTG1 = kThreads / H;               // groups per pass of the CTA
+    static constexpr int kHPT = kPooled ? 2 : 1;            // heads per thread
+    static constexpr int kLPG = H / kHPT;                   // threads (lanes) per group
+    static constexpr int kGPT = kPooled ? H / 2 : 1;        // groups per thread per tile
+    static constexpr int kTG1 = kThreads / kLPG;            // groups per pass of the CTA
     static constexpr int kTG = kTG1 * kGPT;                 // groups per tile
     static constexpr int kGroupFloats = kPooled ? D : kGroup * D;  // stage floats per group
     static constexpr int kStageFloats = kTG * kGroupFloats;
@@ -63,7 +68,7 @@ struct ScoreCfg {
     // stage directly and needs none
     static constexpr int kPoolFloats = kPooled ? 0 : kTG * D;
     static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * size_t(kPoolFloats) * 4 + kStages * 8;
-    static_assert(kThreads % H == 0 && 32 % (4 * H) == 0, "a warp holds whole quads of groups");
+    static_assert(H % kHPT == 0 && kThreads % kLPG == 0 && 32 % (4 * kLPG) == 0, "a warp holds whole quads of groups");
     static_assert(kTG % 4 == 0, "tiles start on quad boundaries");
     static_assert(D % 32 == 0, "the pooled-tile swizzle needs D/4 to be a multiple of 8");
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -157,8 +162,8 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int h = tid % H;       // indexer head of this thread
-    const int gl = tid / H;      // group within the tile
+    const int hl = tid % C::kLPG;  // lane within the group: heads hl * kHPT .. + kHPT - 1
+    const int gl = tid / C::kLPG;  // group within the tile
     // Each CTA walks one contiguous range of tiles: it meets at most a couple
     // of queries (few reloads of q) and streams its keys sequentially.
     const int total = a.batch * tiles_per_q;
@@ -213,7 +218,7 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     if (tid == 0 && !a.no_issue)
         for (int s = 0; s < C::kStages; ++s) issue(s);
 
-    float qreg[D];
+    float qreg[C::kHPT][D];
     int cur_b = -1;
     QueryCache qc;
     int t_cons = t_begin;
@@ -229,14 +234,18 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         float *pool = pooled + (it & 1) * C::kPoolFloats;
 
         if (r.b != cur_b) {
-            const float4 *qp = reinterpret_cast<const float4 *>(a.q_idx + (int64_t(r.b) * H + h) * D);
 #pragma unroll
-            for (int j4 = 0; j4 < F4; ++j4) {
-                const float4 v = __ldg(qp + j4);
-                qreg[4 * j4 + 0] = v.x;
-                qreg[4 * j4 + 1] = v.y;
-                qreg[4 * j4 + 2] = v.z;
-                qreg[4 * j4 + 3] = v.w;
+            for (int u = 0; u < C::kHPT; ++u) {
+                const float4 *qp =
+                    reinterpret_cast<const float4 *>(a.q_idx + (int64_t(r.b) * H + hl * C::kHPT + u) * D);
+#pragma unroll
+                for (int j4 = 0; j4 < F4; ++j4) {
+                    const float4 v = __ldg(qp + j4);
+                    qreg[u][4 * j4 + 0] = v.x;
+                    qreg[u][4 * j4 + 1] = v.y;
+                    qreg[u][4 * j4 + 2] = v.z;
+                    qreg[u][4 * j4 + 3] = v.w;
+                }
             }
             cur_b = r.b;
         }
@@ -264,14 +273,17 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
         // (the pooled form reads its stage in place: one barrier per tile,
         // after the dots, settles a timed-out wait and frees the stage)
 
-        // Dots: groups gl + kTG1 * i of the tile, i < kGPT, each a D-long chain.
+        // Dots: groups gl + kTG1 * i of the tile, i < kGPT, times this
+        // thread's kHPT heads, each a D-long chain.
         const float *tile = kPooled ? stages + size_t(s) * C::kStageFloats : pool;
-        // The kGPT chains advance side by side (independent FMAs to overlap);
-        // rows past the tile's end compute from stale shared memory and are
-        // dropped below.
-        float acc[C::kGPT];
+        // The kGPT x kHPT chains advance side by side (independent FMAs to
+        // overlap); rows past the tile's end compute from stale shared memory
+        // and are dropped below.
+        float acc[C::kGPT][C::kHPT];
 #pragma unroll
-        for (int i = 0; i < C::kGPT; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < C::kGPT; ++i)
+#pragma unroll
+            for (int u = 0; u < C::kHPT; ++u) acc[i][u] = 0.0f;
 #pragma unroll
         for (int j4 = 0; j4 < F4; ++j4) {
             float4 pv[C::kGPT];
@@ -279,17 +291,21 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
             for (int i = 0; i < C::kGPT; ++i)
                 pv[i] = *reinterpret_cast<const float4 *>(tile + pool_index<D>(gl + C::kTG1 * i, j4));
 #pragma unroll
-            for (int i = 0; i < C::kGPT; ++i) {
-                acc[i] = __fmaf_rn(qreg[4 * j4 + 0], pv[i].x, acc[i]);
-                acc[i] = __fmaf_rn(qreg[4 * j4 + 1], pv[i].y, acc[i]);
-                acc[i] = __fmaf_rn(qreg[4 * j4 + 2], pv[i].z, acc[i]);
-                acc[i] = __fmaf_rn(qreg[4 * j4 + 3], pv[i].w, acc[i]);
-            }
+            for (int i = 0; i < C::kGPT; ++i)
+#pragma unroll
+                for (int u = 0; u < C::kHPT; ++u) {
+                    acc[i][u] = __fmaf_rn(qreg[u][4 * j4 + 0], pv[i].x, acc[i][u]);
+                    acc[i][u] = __fmaf_rn(qreg[u][4 * j4 + 1], pv[i].y, acc[i][u]);
+                    acc[i][u] = __fmaf_rn(qreg[u][4 * j4 + 2], pv[i].z, acc[i][u]);
+                    acc[i][u] = __fmaf_rn(qreg[u][4 * j4 + 3], pv[i].w, acc[i][u]);
+                }
         }
-        float relu[C::kGPT];
+        float relu[C::kGPT][C::kHPT];
 #pragma unroll
         for (int i = 0; i < C::kGPT; ++i)
-            relu[i] = (ok && gl + C::kTG1 * i < r.n && acc[i] > 0.0f) ? acc[i] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < C::kHPT; ++u)
+                relu[i][u] = (ok && gl + C::kTG1 * i < r.n && acc[i][u] > 0.0f) ? acc[i][u] : 0.0f;
         if constexpr (kPooled) {
             // the stage has been read by every thread: refill it
             if (__syncthreads_or(!ok)) {
@@ -298,24 +314,26 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
             }
             if (tid == 0 && !a.no_issue) issue(s);
         }
-        const int base = lane & ~(H - 1);
+        const int base = lane & ~(C::kLPG - 1);
 #pragma unroll
         for (int i = 0; i < C::kGPT; ++i) {
             const int g = gl + C::kTG1 * i;
-            // Head sum, h = 0..H-1 in order, gathered from the H lanes of the group.
+            // Head sum, h = 0..H-1 in order, gathered from the kLPG lanes of the
+            // group (head h is component h % kHPT of lane h / kHPT).
             float hv[H];
 #pragma unroll
-            for (int hh = 0; hh < H; ++hh) hv[hh] = __shfl_sync(0xffffffffu, relu[i], base + hh);
+            for (int hh = 0; hh < H; ++hh)
+                hv[hh] = __shfl_sync(0xffffffffu, relu[i][hh % C::kHPT], base + hh / C::kHPT);
             float sum = 0.0f;
 #pragma unroll
             for (int hh = 0; hh < H; ++hh) sum = __fadd_rn(sum, hv[hh]);
-            if (h == 0 && g < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + g] = sum;
-            // Selection hint: the largest key among groups 4j..4j+3 (the H-lane
-            // blocks of those four groups sit side by side in the warp).
+            if (hl == 0 && g < r.n) a.scores[int64_t(r.b) * a.score_stride + r.g0 + g] = sum;
+            // Selection hint: the largest key among groups 4j..4j+3 (the
+            // kLPG-lane blocks of those four groups sit side by side in the warp).
             uint32_t qk = (g < r.n) ? order_key(sum) : 0u;
-            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, H));
-            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, 2 * H));
-            if ((lane & (4 * H - 1)) == 0 && g < r.n)
+            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, C::kLPG));
+            qk = max(qk, __shfl_xor_sync(0xffffffffu, qk, 2 * C::kLPG));
+            if ((lane & (4 * C::kLPG - 1)) == 0 && g < r.n)
                 a.qmax[int64_t(r.b) * a.qmax_stride + ((r.g0 + g) >> 2)] = qk;
         }
 
