@@ -56,17 +56,26 @@ def test_pooled_cache_matches_oracle_bitwise():
         assert got.tobytes() == ref.tobytes(), b
 
 
-@pytest.mark.parametrize("kind", ["paged", "shared_history", "idx4x32"])
+@pytest.mark.parametrize("kind", ["paged", "shared_history", "idx4x32", "idx8x32", "idx4x64"])
 def test_score_pooled_equals_full_raw_bitwise(kind):
+    """The pooled-key scorer (a thread holds two heads and runs H chains over
+    H/2 groups) against the raw-key scorer, bit for bit, on every compiled
+    indexer shape, and against the oracle's incremental scores."""
     torch = need_gpu()
     import oracle
     if kind == "paged":
         w = _paged()
     elif kind == "shared_history":
         w = wl.chunked_prefill_100000(n=12, first=9000)
-    else:
+    elif kind == "idx4x32":
         w = wl.make_workload("inc4", [7777, 4100, 12], idx_heads=4, idx_dim=32, q_heads=4,
                              kv_heads=4, head_dim=64, seed=72, slots="permutation")
+    elif kind == "idx8x32":
+        w = wl.make_workload("inc8x32", [6001, 4099, 513, 3], idx_heads=8, idx_dim=32, q_heads=8,
+                             kv_heads=2, head_dim=64, seed=73, slots="paged16")
+    else:
+        w = wl.make_workload("inc4x64", [8191, 1030, 77], idx_heads=4, idx_dim=64, q_heads=2,
+                             kv_heads=2, head_dim=64, seed=74, slots="identity")
     db = _batch(w)
     db.score()
     torch.cuda.synchronize()

@@ -4,9 +4,10 @@ ABI: qsa_score_groups_shared and qsa_decode_shared.
 "Top-k chooses the set; time chooses the order" (AFN-017) requires chunk =
 decode: a query of a chunked prefill must see exactly what a single-query
 decode at its position sees.  The shared scorer pools each tile of the
-history once for many queries and splits every FMA chain across lanes, so
-its scores, rows and outputs are checked bit for bit against the per-query
-path (itself checked against the oracle elsewhere)."""
+history once for many queries (one lane per query, two heads per lane, the
+head sums in a second pass), so its scores, rows and outputs are checked bit
+for bit against the per-query path (itself checked against the oracle
+elsewhere)."""
 import numpy as np
 import pytest
 
@@ -57,6 +58,21 @@ def test_shared_scores_and_decode_equal_per_query(shape):
     vis = [9001 + 7 * i for i in range(34)] + [37, 2052, 4 * 777 + 3]
     w = wl.make_workload("shared", vis, idx_heads=H, idx_dim=dI, q_heads=nq, kv_heads=nkv, head_dim=hd,
                          seed=81 + H * dI, history="shared", slots="paged16")
+    db = qsa.DeviceBatch(w)
+    _scores_equal(db, w)
+    _decode_equal(db, w)
+
+
+@pytest.mark.parametrize("nq", [150, 65])
+def test_shared_partial_last_query_block(nq):
+    """Batches of several 64-query blocks whose last block is partial (150 =
+    64 + 64 + 22; 65 = 64 + 1): the blocks get CTAs in proportion to their
+    queries, and every query's scores and rows equal the per-query path."""
+    need_gpu()
+    from top_group_sparse_gb300 import qsa
+    vis = [4000 + 13 * i for i in range(nq - 2)] + [2051, 4 * 1001]
+    w = wl.make_workload("shared_blocks", vis, idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2, head_dim=128,
+                         seed=91 + nq, history="shared", slots="paged16")
     db = qsa.DeviceBatch(w)
     _scores_equal(db, w)
     _decode_equal(db, w)
