@@ -500,7 +500,7 @@ def run_gpu(args):
     # ---- the batched decode: 32 queries x 65,537 visible tokens ------------------
     batched = None
     if not args.no_batched:
-        w3 = wl.batched_65537()
+        w3 = wl.batched_65537(batch=args.batched_queries)
         d3 = qsa.DeviceBatch(w3, device=f"cuda:{local}")
 
         def step3(s):
@@ -652,6 +652,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill side measurement")
     ap.add_argument("--no-batched", action="store_true", help="skip the 32 x 65,537 batched-decode measurement")
+    ap.add_argument("--batched-queries", type=int, default=32,
+                    help="queries of the batched-decode measurement (32: the workload; fewer for small profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
