@@ -176,6 +176,9 @@ score_groups_kernel(const ScoreArgs a, const int tiles_per_q)
     const uint64_t t_start = global_timer_ns();
 
     allow_successor_launch();  // selection CTAs fill SMs as this grid's CTAs retire
+    // The pooled form may be launched while the kernel before it (the append
+    // of new groups to the cache) finishes: wait for it before any input.
+    if constexpr (kPooled) wait_for_predecessor();
     if (blockIdx.x == 0) {
         for (int b = tid; b < a.batch; b += blockDim.x) {
             const int T = __ldg(a.visible + b);
@@ -402,6 +405,9 @@ cudaError_t launch_score_t(const ScoreArgs &a, int num_sms, cudaStream_t s)
         (void)cudaGetLastError();
         ab.bal_coop = 0;
     }
+    if constexpr (kPooled)  // its launch overlaps the tail of the kernel before it
+        return launch_kernel(score_groups_kernel<H, D, kPooled>, dim3(unsigned(grid)), dim3(C::kThreads), C::kSmem, s,
+                             true, ab, tiles_per_q);
     score_groups_kernel<H, D, kPooled><<<grid, C::kThreads, C::kSmem, s>>>(ab, tiles_per_q);
     return cudaGetLastError();
 }
@@ -421,6 +427,7 @@ __global__ void __launch_bounds__(kPoolThreads)
 pool_groups_kernel(const PoolArgs a)
 {
     constexpr int F4 = D / 4;
+    allow_successor_launch();  // a scorer launched after this append may start its launch now
     const int b = blockIdx.y;
     const int g_begin = __ldg(a.group_begin + b), g_end = __ldg(a.group_end + b);
     if (g_begin < 0 || g_end < g_begin || g_end > a.g_max || g_end - g_begin > a.max_groups) {
