@@ -346,7 +346,10 @@ qsa_status qsa_pool_groups(const qsa_dims *dims, const qsa_inputs *in, const int
 /* qsa_score_groups with the pooled keys read from the cache (rows
  * pool_offset[b] + g, g < floor(T_b/4)) instead of pooled from the raw keys:
  * G*d_I*4 bytes streamed per query instead of T*d_I*4.  Reads in->q_idx and
- * in->visible; in->idx_keys and in->key_offset may be NULL. */
+ * in->visible; in->idx_keys and in->key_offset may be NULL.  Its kernel is
+ * launched with programmatic dependent launch: it may start while the kernel
+ * before it on `stream` (e.g. qsa_pool_groups) finishes, and waits for that
+ * kernel to complete before it reads anything, so stream order holds. */
 qsa_status qsa_score_pooled(const qsa_dims *dims, const qsa_inputs *in, const float *pooled,
                             const int64_t *pool_offset, float *scores, void *ws, size_t ws_bytes,
                             void *stream);
