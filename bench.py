@@ -44,6 +44,7 @@ PROFILE = os.path.join(ROOT, "profiles", "score_groups_long_262144.md")
 SCORE_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score.cu")
 ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_long_262144.md")
 ATTEND_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "attend.cu")
+ATTEND_BATCHED_PROFILE = os.path.join(ROOT, "profiles", "attend_batched_65537.md")
 
 
 def config_dict(w):
@@ -519,7 +520,9 @@ def run_gpu(args):
             "value": ws * w3.batch / (ms3 * 1e-3), "unit": UNIT, "ms_per_step": ms3, "steps": K3,
             "roofline": hbm_roofline("score_groups", s3, st3[0], peak, peak_src, None,
                                      f"algorithmic bytes {s3} per launch (raw index keys + indexer queries)"),
-            "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(w3), st3[2], peak, peak_src, None,
+            "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(w3), st3[2], peak, peak_src,
+                                            profile_traffic(ATTEND_BATCHED_PROFILE, ATTEND_SRC)
+                                            if w3.batch == 32 else None,
                                             "selected K/V rows + slot entries + queries + outputs"),
             "path_hbm": {"achieved_gbs": p3 / (ms3 * 1e-3) / 1e9, "frac_of_measured": p3 / (ms3 * 1e-3) / 1e9 / peak,
                          "frac_of_8tbs": p3 / (ms3 * 1e-3) / 1e9 / 8000.0, "algorithmic_bytes_per_step": p3},
