@@ -45,6 +45,8 @@ SCORE_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score.cu")
 ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_long_262144.md")
 ATTEND_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "attend.cu")
 ATTEND_BATCHED_PROFILE = os.path.join(ROOT, "profiles", "attend_batched_65537.md")
+SHARED_PROFILE = os.path.join(ROOT, "profiles", "score_shared_chunked_prefill_100000.md")
+SHARED_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score_shared.cu")
 
 
 def config_dict(w):
@@ -560,10 +562,10 @@ def run_gpu(args):
         fma_attend = attend_fma(wc)
         key_bytes = int(wc.visible.max()) * wc.idx_dim * 4  # the shared history, streamed once
 
-        def alu_roofline(kernel, ms):
+        def alu_roofline(kernel, ms, traffic=None):
             tf = 2 * fma_score / (ms * 1e-3) / 1e12
             return {"kernel": kernel, "bound": "alu", "achieved": tf, "peak": ffma["tflops"], "unit": "TFLOP/s",
-                    "frac": tf / ffma["tflops"], "traffic": None, "us_per_launch": ms * 1e3,
+                    "frac": tf / ffma["tflops"], "traffic": traffic, "us_per_launch": ms * 1e3,
                     "fma_per_launch": fma_score, "peak_source": "measured in this run: " + ffma["how"],
                     "hbm_frac": key_bytes / (ms * 1e-3) / 1e9 / peak}
 
@@ -571,7 +573,8 @@ def run_gpu(args):
         if solo and rank == 0:
             cpu_c = oracle_pair(wc, list(range(wc.batch)))
         shared = {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared,
-                  "roofline": alu_roofline("score_shared_kernel (qsa_score_groups_shared)", ms_scorer_shared),
+                  "roofline": alu_roofline("score_shared_kernel (qsa_score_groups_shared)", ms_scorer_shared,
+                                           profile_traffic(SHARED_PROFILE, SHARED_SRC)),
                   "step_fma": fma_score + fma_attend,
                   "step_frac": 2 * (fma_score + fma_attend) / (ms_shared * 1e-3) / 1e12 / ffma["tflops"]}
         per_query = {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single,
