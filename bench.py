@@ -46,6 +46,7 @@ ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_long_262144.md")
 ATTEND_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "attend.cu")
 ATTEND_BATCHED_PROFILE = os.path.join(ROOT, "profiles", "attend_batched_65537.md")
 SHARED_PROFILE = os.path.join(ROOT, "profiles", "score_shared_chunked_prefill_100000.md")
+SCORE_BATCHED_PROFILE = os.path.join(ROOT, "profiles", "score_groups_batched_65537.md")
 SHARED_SRC = os.path.join(ROOT, "top_group_sparse_gb300", "csrc", "score_shared.cu")
 
 
@@ -520,7 +521,8 @@ def run_gpu(args):
         batched = {
             "workload": "batched_65537", "queries_per_step": w3.batch, "visible_tokens": int(w3.visible[0]),
             "value": ws * w3.batch / (ms3 * 1e-3), "unit": UNIT, "ms_per_step": ms3, "steps": K3,
-            "roofline": hbm_roofline("score_groups", s3, st3[0], peak, peak_src, None,
+            "roofline": hbm_roofline("score_groups", s3, st3[0], peak, peak_src,
+                                     profile_traffic(SCORE_BATCHED_PROFILE) if w3.batch == 32 else None,
                                      f"algorithmic bytes {s3} per launch (raw index keys + indexer queries)"),
             "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(w3), st3[2], peak, peak_src,
                                             profile_traffic(ATTEND_BATCHED_PROFILE, ATTEND_SRC)
