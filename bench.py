@@ -543,9 +543,9 @@ def run_gpu(args):
         wc = wl.chunked_prefill_100000()
         dc = qsa.DeviceBatch(wc, device=f"cuda:{local}")
 
-        def time_path(fn, n=50):
+        def time_path(fn, n=50):  # ms per launch, the slowest rank's
             tm.warm(fn, 3)
-            return float(tm.run(fn, n).mean())
+            return max_over_ranks(float(tm.run(fn, n).mean()), dev)
 
         ms_shared = time_path(dc.decode_shared)
         ms_single = time_path(dc.decode)
@@ -574,12 +574,12 @@ def run_gpu(args):
         cpu_c = None
         if solo and rank == 0:
             cpu_c = oracle_pair(wc, list(range(wc.batch)))
-        shared = {"value": wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared,
+        shared = {"value": ws * wc.batch / (ms_shared * 1e-3), "unit": UNIT, "ms_per_step": ms_shared,
                   "roofline": alu_roofline("score_shared_kernel (qsa_score_groups_shared)", ms_scorer_shared,
                                            profile_traffic(SHARED_PROFILE, SHARED_SRC)),
                   "step_fma": fma_score + fma_attend,
                   "step_frac": 2 * (fma_score + fma_attend) / (ms_shared * 1e-3) / 1e12 / ffma["tflops"]}
-        per_query = {"value": wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single,
+        per_query = {"value": ws * wc.batch / (ms_single * 1e-3), "unit": UNIT, "ms_per_step": ms_single,
                      "roofline": alu_roofline("score_groups_kernel (qsa_score_groups; each query streams "
                                               "its own keys, mostly from L2)", ms_scorer_single),
                      "roofline_attend": hbm_roofline("attend_kernel", attend_bytes(wc), stc[2], peak, peak_src,
