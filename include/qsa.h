@@ -68,9 +68,10 @@ typedef enum {
 /* Problem dimensions.  Supported builds: (idx_heads, idx_dim) in
  * {(4,32), (8,32), (4,64), (8,64)}; head_dim in {64, 128};
  * q_heads = kv_heads * r with r in 1..16; group == 4; 1 <= budget_groups
- * <= 512; 0 <= max_visible <= QSA_MAX_VISIBLE. */
+ * <= 512; 0 <= max_visible <= QSA_MAX_VISIBLE; 0 <= batch <= 65535 (the
+ * attention's grids carry the query in a dimension of at most 65,535). */
 typedef struct {
-    int32_t batch;          /* B: decode queries in this call (>= 0)              */
+    int32_t batch;          /* B: decode queries in this call (0..65535)          */
     int32_t idx_heads;      /* H_I: indexer query heads                          */
     int32_t idx_dim;        /* d_I: width of one raw index key                   */
     int32_t q_heads;        /* n_q: attention query heads                        */

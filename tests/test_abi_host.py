@@ -85,6 +85,8 @@ def test_invalid_dims_give_zero_workspace(lib):
     assert qsa.qsa_workspace_size(_dims(budget_groups=513)) == 0
     assert qsa.qsa_workspace_size(_dims(q_heads=15)) == 0
     assert qsa.qsa_workspace_size(_dims(batch=-1)) == 0
+    assert qsa.qsa_workspace_size(_dims(batch=65536)) == 0  # grids carry the query in a 16-bit dimension
+    assert qsa.qsa_workspace_size(_dims(batch=65535, max_visible=64)) > 0
     assert qsa.qsa_workspace_size(_dims(max_visible=(1 << 26) + 1)) == 0
 
 
