@@ -46,3 +46,29 @@ def test_max_visible_history_and_keys_past_2_31_elements():
     assert gpu["n_ids"].tolist() == [2048, 2051]
     del w, gpu, ref
     gc.collect()
+
+
+def test_max_batch_of_65535_queries():
+    """The largest accepted batch (65,535 queries: the attention grid's query
+    dimension and its merge launch at their limit, a selection grid of
+    65,535 CTAs): T_b = b mod 41 (no groups, dense rows below the budget),
+    every 1,000th query T = 5,000 + b mod 4 (top-k with a tail).  ID rows
+    bit-exact and outputs within 1e-5 * max|V| for every query."""
+    need_gpu()
+    from top_group_sparse_gb300 import qsa
+    B = 65535
+    vis = [5000 + b % 4 if b % 1000 == 999 else b % 41 for b in range(B)]
+    w = wl.make_workload("maxbatch", vis, idx_heads=4, idx_dim=32, q_heads=2, kv_heads=1, head_dim=64,
+                         seed=124, slots="paged16")
+    db = qsa.DeviceBatch(w)
+    gpu = run_decode(w, db=db)
+    gpu.pop("batch")
+    assert gpu["status"] == 0, f"device error flags {gpu['flags']:#x}"
+    del db
+    gc.collect()
+    ref = oracle_run(w)
+    assert_ids_equal(w, gpu, ref)
+    assert_attention_close(w, gpu, ref)
+    assert gpu["n_ids"].tolist() == [4 * min(t // 4, 512) + t % 4 for t in vis]
+    del w, gpu, ref
+    gc.collect()
