@@ -29,6 +29,8 @@
  * - Host-detectable errors (NULL or misaligned pointers, bad dimensions,
  *   unsupported shapes, a workspace that is too small) return a status
  *   before anything is enqueued.  A failed launch returns QSA_ERR_CUDA.
+ *   An empty batch (B = 0) with valid arguments enqueues nothing and
+ *   returns QSA_OK.
  * - Errors that only the device can see (a T_b outside [0, max_visible],
  *   a slot outside [0, num_slots), an ID row longer than its capacity, a
  *   bounded wait that ran out) never trap: the kernel skips the bad access,

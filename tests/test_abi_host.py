@@ -267,3 +267,36 @@ def test_plain_c_client_links_and_calls_the_abi(lib, tmp_path):
     assert int(out[4]) == 8 * 262144 * 64 * 4         # the raw keys the scorer streams
     assert int(out[5]) == 0                           # no query-by-key mask
     assert int(out[6]) == 0 and out[7] == "named"
+
+
+def test_empty_batch_enqueues_nothing(lib):
+    """B = 0: every compute call checks its arguments and returns OK without
+    any CUDA call -- so it succeeds on this machine, which has no GPU.  The
+    device pointers (aligned, never dereferenced) and the workspace size are
+    those a caller would pass."""
+    import ctypes
+    L = qsa.load()
+    d = _dims(batch=0, max_visible=1000)
+    fake = 1 << 20
+    inp = qsa.QsaInputs(q_idx=fake, idx_keys=fake, key_offset=fake, visible=fake, q=fake, k_cache=fake,
+                        v_cache=fake, num_slots=1000, slot_map=fake, slot_offset=fake)
+    ws_bytes = L.qsa_workspace_size(ctypes.byref(d))
+    assert ws_bytes > 0
+    for name in ("qsa_score_groups", "qsa_select", "qsa_gather", "qsa_attend", "qsa_gather_attend",
+                 "qsa_attend_state", "qsa_decode", "qsa_decode_pooled", "qsa_decode_shared", "qsa_pool_groups",
+                 "qsa_score_pooled", "qsa_score_groups_shared"):
+        fn = getattr(L, name)
+        args = []
+        for t in fn.argtypes:
+            if t is ctypes.c_size_t:
+                args.append(ws_bytes)
+            elif t in (ctypes.c_int32, ctypes.c_int, ctypes.c_int64):
+                args.append(0)
+            elif getattr(t, "_type_", None) is qsa.QsaDims:
+                args.append(ctypes.byref(d))
+            elif getattr(t, "_type_", None) is qsa.QsaInputs:
+                args.append(ctypes.byref(inp))
+            else:
+                args.append(ctypes.c_void_p(fake))
+        args[-1] = None  # the legacy default stream
+        assert fn(*args) == qsa.QSA_OK, name
