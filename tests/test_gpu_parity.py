@@ -403,3 +403,40 @@ def test_multi_wave_grid_flags_a_bad_row_and_keeps_the_rest():
         one = qsa.DeviceBatch(w, queries=[b])
         one.decode()
         assert one.out.cpu().numpy()[0].tobytes() == out[b].tobytes(), b
+
+
+def test_non_finite_index_keys_match_the_oracle():
+    """Index keys with +inf, -inf and NaN planted (the reading ReLU(x) = x > 0
+    ? x : +0 keeps every score in [+0, +inf]): 600 groups per history get a
+    +inf element -- more than the budget, so the selection must take the 512
+    earliest of the tied +inf scores -- others -inf, NaN, or +inf and -inf in
+    one group.  Scores and ID rows bit-exact, outputs within 1e-5 * max|V|."""
+    torch = need_gpu()
+    from top_group_sparse_gb300 import qsa
+    from gpu_helpers import assert_scores_equal
+    w = wl.make_workload("nonfinite", [20000, 9001, 3002], idx_heads=8, idx_dim=64, q_heads=16, kv_heads=2,
+                         head_dim=128, seed=131, slots="paged16")
+    rng = np.random.default_rng(7)
+    for b in range(w.batch):
+        base, G = int(w.key_offset[b]), int(w.visible[b]) // 4
+        g = rng.permutation(G)
+        rows = lambda gs: base + 4 * gs + rng.integers(0, 4, gs.shape[0])  # noqa: E731
+        cols = lambda gs: rng.integers(0, w.idx_dim, gs.shape[0])  # noqa: E731
+        gi, gm, gn, gp = g[:600], g[600:650], g[650:700], g[700:750]
+        w.idx_keys[rows(gi), cols(gi)] = np.inf
+        w.idx_keys[rows(gm), cols(gm)] = -np.inf
+        w.idx_keys[rows(gn), cols(gn)] = np.nan
+        c = cols(gp)
+        w.idx_keys[base + 4 * gp, c] = np.inf
+        w.idx_keys[base + 4 * gp + 1, c] = -np.inf
+    db = qsa.DeviceBatch(w)
+    gpu = run_decode(w, db=db)
+    assert gpu["status"] == 0, f"device error flags {gpu['flags']:#x}"
+    db.score()
+    torch.cuda.synchronize()
+    gpu["scores"] = db.scores.cpu().numpy()
+    ref = oracle_run(w)
+    assert_scores_equal(w, gpu, ref)
+    assert np.isinf(ref["scores"][0, :5000]).sum() > 512  # the tie among +inf decides the set
+    assert_ids_equal(w, gpu, ref)
+    assert_attention_close(w, gpu, ref)

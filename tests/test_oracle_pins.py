@@ -175,6 +175,32 @@ def test_scores_exact_on_integer_grid(oracle):
     assert len(np.unique(s0)) < len(s0)
 
 
+def test_non_finite_keys_follow_the_relu_reading(oracle):
+    """Non-finite index keys.  The pages are silent on them; the reading is
+    ReLU(x) = x > 0 ? x : +0, so scores lie in [+0, +inf].  With positive
+    query weights: a +inf pooled element gives +inf dots and a +inf score, a
+    -inf one -inf dots and ReLU +0, NaN (a NaN key, or +inf and -inf pooled
+    together) ReLU +0.  The selection ranks +inf above every finite score and
+    breaks ties among +inf by position."""
+    d = 4
+    q = np.array([[1.0, 1.0, 1.0, 1.0], [0.5, 0.5, 0.5, 0.5]], np.float32)
+    keys = np.zeros((7 * 4, d), np.float32)
+    keys[0:4] = 1.0                         # group 0: pooled 1 -> dots 4, 2 -> 6
+    keys[4, 0] = np.inf                     # group 1: +inf
+    keys[8, 1] = -np.inf                    # group 2: -inf dots -> +0
+    keys[12, 2] = np.nan                    # group 3: NaN dots -> +0
+    keys[16, 0], keys[17, 0] = np.inf, -np.inf  # group 4: inf - inf = NaN -> +0
+    keys[20, 3] = np.inf                    # group 5: +inf
+    keys[24:28] = 2.0                       # group 6: pooled 2 -> dots 8, 4 -> 12
+    scores = oracle.score_groups(q, keys)
+    want = np.array([6.0, np.inf, 0.0, 0.0, 0.0, np.inf, 12.0], np.float32)
+    assert scores.tobytes() == want.tobytes()
+    _, chosen = oracle.select(scores, keys.shape[0], 3, return_chosen=True)
+    assert chosen.tolist() == [1, 5, 6]
+    _, chosen = oracle.select(scores, keys.shape[0], 1, return_chosen=True)
+    assert chosen.tolist() == [1]       # the +inf tie goes to the earlier group
+
+
 def test_relu_before_head_sum_matters(oracle):
     """Order check on a hand case: heads with dots +1 and -1 give 1, not 0."""
     q = np.array([[1.0, 0.0], [-1.0, 0.0]], np.float32)
